@@ -1,0 +1,486 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused N-way reduce + residual add + RMSNorm (+ per-token FP8) path.
+
+Metric: microseconds per call under CUDA-graph replay, and the achieved HBM bandwidth of
+the fused kernel as a fraction of the measured GB300 copy bandwidth.
+
+Headline workload: N=4 bf16 partials of 2800 x 6144, residual in/out, gemma (1 + w)
+RMSNorm, per-token FP8 E4M3 codes with fp32 scales and the bf16 mirror, i.e. every step of
+the path in one call.  A "step" is one replay of a CUDA graph holding `calls_per_step`
+calls that rotate over buffer sets larger than L2 together, the methodology of the pages'
+benchmarks (k calls captured per graph, replays timed with CUDA events).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs an independent replica on its own GPU (the path has no
+exchange between GPUs); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+HEADLINE = "n4_m2800_h6144_bf16_gemma_fp8"
+METRIC = "us/call (CUDA-graph replay) and achieved HBM GB/s, fused reduce+RMSNorm"
+UNIT = "us/call"
+SMI_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+# ---------------------------------------------------------------------------
+# ranks (replicas)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend)
+    return dist
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the slowest replica sets the job's time)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_us_per_call(max_elapsed_ms: float, calls_per_rank: int, world: int) -> float:
+    """Whole-job time per call: the slowest rank's elapsed time over all calls of all ranks."""
+    return max_elapsed_ms * 1000.0 / (calls_per_rank * world)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
+        self.gpu, self.interval, self.proc, self.path = gpu_index, interval_ms, None, None
+
+    def start(self):
+        import shutil
+        import tempfile
+        if not shutil.which("nvidia-smi"):
+            return
+        fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+        os.close(fd)
+        self.proc = subprocess.Popen(
+            ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
+             "-lms", str(self.interval)], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        time.sleep(self.interval / 1000.0 * 2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    frac = float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts + frac, float(parts[2]), float(parts[3]), parts[5:]))
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        window = "timed"
+        if not inside:
+            inside, window = rows, "run (no sample fell inside the timed region)"
+        if not inside:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3][1:5]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+# ---------------------------------------------------------------------------
+# our path
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "tensor_all_reduce_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernels."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = kernel_source_hash()
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or not line.strip():
+                continue
+            kv = dict(tok.split("=", 1) for tok in line.split())
+            if kv.get("workload") == workload and kv.get("kernel_src") == cur:
+                return int(kv["bytes_per_launch"])
+    return None
+
+
+class FusedSets:
+    """R buffer sets for one fused workload, carved from one slab per role."""
+
+    def __init__(self, wl, sets: int, dev):
+        import torch
+        from tensor_all_reduce_gb300 import synth
+        self.wl, self.R = wl, sets
+        t = synth.TORCH_DTYPES[wl.dtype]
+        m, h, n = wl.m, wl.h, wl.n
+        inp = wl.inputs()
+        self.parts = torch.empty((sets, n, m, h), dtype=t, device=dev)
+        self.res = torch.empty((sets, m, h), dtype=t, device=dev) if wl.residual else None
+        self.w = inp["weight"].to(dev)
+        want_y = wl.mirror or not wl.quant
+        self.out = torch.empty((sets, m, h), dtype=t, device=dev) if want_y else None
+        self.ro = torch.empty((sets, m, h), dtype=t, device=dev) if wl.residual else None
+        self.q = torch.empty((sets, m, h), dtype=torch.uint8, device=dev) if wl.quant else None
+        self.sc = torch.empty((sets, m), dtype=torch.float32, device=dev) if wl.quant else None
+        for k in range(n):
+            self.parts[:, k].copy_(inp["partials"][k].to(dev).unsqueeze(0).expand(sets, m, h))
+        if self.res is not None:
+            self.res.copy_(inp["residual"].to(dev).unsqueeze(0).expand(sets, m, h))
+
+    def call(self, ctx, i: int):
+        r = i % self.R
+        wl = self.wl
+        ctx.fused_reduce_rmsnorm(list(self.parts[r].unbind(0)), None if self.res is None else self.res[r], self.w,
+                                 eps=1e-6, gemma=wl.gemma, quant=wl.quant,
+                                 out=None if self.out is None else self.out[r],
+                                 residual_out=None if self.ro is None else self.ro[r],
+                                 q_out=None if self.q is None else self.q[r],
+                                 scale_out=None if self.sc is None else self.sc[r],
+                                 want_out=self.out is not None, want_residual_out=self.ro is not None)
+
+
+class ReduceSets:
+    def __init__(self, wl, sets: int, dev):
+        import torch
+        from tensor_all_reduce_gb300 import synth
+        self.wl, self.R = wl, sets
+        t = synth.TORCH_DTYPES[wl.dtype]
+        parts = synth.reduce_inputs(wl.n, wl.numel, wl.dtype, wl.seed)
+        self.parts = torch.empty((sets, wl.n, wl.numel), dtype=t, device=dev)
+        for k in range(wl.n):
+            self.parts[:, k].copy_(parts[k].to(dev).unsqueeze(0).expand(sets, wl.numel))
+        self.out = torch.empty((sets, wl.numel), dtype=t, device=dev)
+
+    def call(self, ctx, i: int):
+        r = i % self.R
+        ctx.reduce_sum(list(self.parts[r].unbind(0)), out=self.out[r])
+
+
+def rotation_sets(footprint: int, l2: int, cap: int = 4096) -> int:
+    """Buffer sets whose total footprint covers L2 three times (HBM-cold replays)."""
+    return max(1, min(cap, math.ceil(3 * l2 / max(footprint, 1))))
+
+
+def time_graph(sets, ctx, calls: int, steps: int, warmup: int, world: int, sampler=None):
+    """Capture `calls` calls in one graph; replay `warmup` untimed, then time `steps` replays."""
+    import torch
+    for i in range(min(calls, sets.R)):
+        sets.call(ctx, i)                   # eager warm-up of every buffer set
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=s):
+        for i in range(calls):
+            sets.call(ctx, i)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record()
+    for _ in range(steps):
+        g.replay()
+    end.record()
+    end.synchronize()
+    t1 = time.time()
+    torch.cuda.synchronize()
+    barrier(world)
+    elapsed_ms = start.elapsed_time(end)
+    del g
+    return elapsed_ms, t0, t1
+
+
+def e2e_fused(ctx, wl, steps: int, dev):
+    """Same metric end to end: pinned host inputs -> device, the fused call, outputs -> pinned host."""
+    import torch
+    from tensor_all_reduce_gb300 import synth
+    inp = wl.inputs()
+    t = synth.TORCH_DTYPES[wl.dtype]
+    m, h = wl.m, wl.h
+    h_parts = [p.pin_memory() for p in inp["partials"]]
+    h_res = inp["residual"].pin_memory() if inp["residual"] is not None else None
+    h_w = inp["weight"].pin_memory()
+    d_parts = [torch.empty((m, h), dtype=t, device=dev) for _ in range(wl.n)]
+    d_res = torch.empty((m, h), dtype=t, device=dev) if h_res is not None else None
+    d_w = torch.empty((h,), dtype=t, device=dev)
+    d_out = torch.empty((m, h), dtype=t, device=dev)
+    d_ro = torch.empty((m, h), dtype=t, device=dev) if h_res is not None else None
+    d_q = torch.empty((m, h), dtype=torch.uint8, device=dev) if wl.quant else None
+    d_sc = torch.empty((m,), dtype=torch.float32, device=dev) if wl.quant else None
+    outs_d = [x for x in (d_out, d_ro, d_q, d_sc) if x is not None]
+    outs_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs_d]
+    h2d = sum(x.numel() * x.element_size() for x in h_parts + [h_w] + ([h_res] if h_res is not None else []))
+    d2h = sum(x.numel() * x.element_size() for x in outs_d)
+
+    def step():
+        for d, hh in zip(d_parts, h_parts):
+            d.copy_(hh, non_blocking=True)
+        if d_res is not None:
+            d_res.copy_(h_res, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        ctx.fused_reduce_rmsnorm(d_parts, d_res, d_w, eps=1e-6, gemma=wl.gemma, quant=wl.quant, out=d_out,
+                                 residual_out=d_ro, q_out=d_q, scale_out=d_sc,
+                                 want_residual_out=d_ro is not None)
+        for hh, d in zip(outs_h, outs_d):
+            hh.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        step()
+    end.record()
+    end.synchronize()
+    return start.elapsed_time(end) * 1000.0 / steps, h2d, d2h
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_us(wl, rows: int):
+    """Time the oracle on the first `rows` rows of the workload; returns (us per full call, rows)."""
+    import oracle
+    from tensor_all_reduce_gb300 import synth
+    rows = max(1, min(rows, wl.m))
+    inp = synth.fused_inputs(wl.n, rows, wl.h, wl.dtype, seed=wl.seed, gemma=wl.gemma, residual=wl.residual)
+    orc = oracle.get()
+    args = ([synth.bits(p) for p in inp["partials"]], synth.bits(inp["residual"]), synth.bits(inp["weight"]),
+            1e-6, wl.gemma, wl.quant, wl.dtype)
+    t = time.perf_counter()
+    orc.fused(*args)
+    dt = time.perf_counter() - t
+    return dt * 1e6 * (wl.m / rows), rows
+
+
+def cpu_baseline(wl, seconds: float = 12.0):
+    """Serial oracle (one thread), timed on a bounded sample of the workload's rows."""
+    us1, rows = oracle_sample_us(wl, 16)                 # size the sample
+    per_row_s = us1 / 1e6 / wl.m
+    rows = max(16, min(wl.m, int(seconds / 3 / per_row_s)))
+    samples = [oracle_sample_us(wl, rows)[0] for _ in range(3)]
+    return {"value": statistics.median(samples), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"serial C oracle on {rows} of {wl.m} rows, median of 3 runs, scaled to a full call"}
+
+
+def run_reference(args, world, rank):
+    from tensor_all_reduce_gb300 import synth
+    if rank != 0:
+        return 0
+    wl = synth.by_name(args.workload)
+    us1, _ = oracle_sample_us(wl, 8)
+    # size each step so that warm-up + steps stay within about two minutes
+    budget_s = min(120.0, 1.0 * (args.steps + args.warmup))
+    rows = max(1, min(wl.m, int(budget_s / (args.steps + args.warmup) / (us1 / 1e6 / wl.m))))
+    for _ in range(args.warmup):
+        oracle_sample_us(wl, rows)
+    times = [oracle_sample_us(wl, rows)[0] for _ in range(args.steps)]
+    value = statistics.median(times)
+    sample = f"serial C oracle on {rows} of {wl.m} rows per step, scaled to a full call; median of {args.steps} steps"
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sum(times) / len(times) / 1000, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
+            "data": "synthetic", "config": {"workload": wl.name, "n_partials": wl.n, "m": wl.m, "h": wl.h},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# main
+# ---------------------------------------------------------------------------
+
+def sweep(ctx, dev, l2, peak):
+    """Every workload family once (short): us/call cold (rotating sets) and warm (one set)."""
+    import torch
+    from tensor_all_reduce_gb300 import synth
+    out = []
+    for wl in synth.all_fused() + synth.reduce_only():
+        fused = isinstance(wl, synth.FusedWorkload)
+        fp = wl.algorithmic_bytes()
+        R = rotation_sets(fp, l2)
+        calls = max(64, R)
+        sets = (FusedSets if fused else ReduceSets)(wl, R, dev)
+        ms, _, _ = time_graph(sets, ctx, calls, steps=5, warmup=2, world=1)
+        cold = ms * 1000 / (5 * calls)
+        variant = ctx.last_variant
+        del sets
+        torch.cuda.empty_cache()
+        sets = (FusedSets if fused else ReduceSets)(wl, 1, dev)
+        ms, _, _ = time_graph(sets, ctx, 64, steps=5, warmup=2, world=1)
+        warm = ms * 1000 / (5 * 64)
+        del sets
+        torch.cuda.empty_cache()
+        gbs = fp / (cold * 1e-6) / 1e9
+        out.append({"workload": wl.name, "variant": variant, "us_per_call_cold": round(cold, 3),
+                    "us_per_call_l2_warm": round(warm, 3), "bytes_per_call": fp, "gbs_cold": round(gbs, 1),
+                    "frac_of_peak_cold": round(gbs / peak, 4), "rotation_sets": R})
+    return out
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=100)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    p.add_argument("--workload", default=HEADLINE)
+    p.add_argument("--calls-per-step", type=int, default=500)
+    p.add_argument("--no-sweep", action="store_true", help="skip the per-workload sweep")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    args = p.parse_args(argv)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+
+    import torch
+    import tensor_all_reduce_gb300 as tar
+    from tensor_all_reduce_gb300 import synth
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    import __graft_entry__
+    if rank == 0:
+        __graft_entry__.build()
+    barrier(world)
+    ctx = tar.Context(local)
+    l2 = ctx.info(tar.AR_INFO_L2_BYTES)
+    peak, peak_kind = measured_peaks()
+    wl = synth.by_name(args.workload)
+    fp = wl.algorithmic_bytes()
+    R = rotation_sets(fp, l2, cap=64)
+    calls = max(args.calls_per_step, R)
+    sets = FusedSets(wl, R, dev)
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    elapsed_ms, t0, t1 = time_graph(sets, ctx, calls, args.steps, args.warmup, world)
+    clocks = sampler.stop(t0, t1) if sampler else None
+    variant = ctx.last_variant
+    max_ms = max_over_ranks(elapsed_ms, world, dev)
+    launches = args.steps * calls
+    value = job_us_per_call(max_ms, launches, world)
+    per_launch_us = elapsed_ms * 1000.0 / launches          # this rank's average launch duration
+    achieved = fp / (per_launch_us * 1e-6) / 1e9
+    del sets
+    torch.cuda.empty_cache()
+
+    e2e_us, h2d, d2h = e2e_fused(ctx, wl, args.e2e_steps, dev)
+    e2e_us = max_over_ranks(e2e_us, world, dev) / world
+
+    extra = {}
+    if rank == 0 and not args.no_sweep:
+        extra["sweep"] = sweep(ctx, dev, l2, peak)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl)
+    ctx.close()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": {"workload": wl.name, "n_partials": wl.n, "m": wl.m, "h": wl.h, "gemma": wl.gemma,
+                       "fp8_per_token": wl.quant, "bf16_mirror": wl.mirror, "calls_per_step": calls,
+                       "buffer_sets": R, "l2": f"inputs larger than L2 ({fp / 1e6:.0f} MB per call vs "
+                                                f"{l2 / 1e6:.0f} MB L2), {R} rotating buffer sets",
+                       "parallelism": "replicas" if world > 1 else "single GPU", "variant": variant},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name),
+                         "peak_kind": peak_kind, "algorithmic_bytes_per_launch": fp},
+            "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "note": "one call per step: inputs copied from pinned host memory, outputs copied back"},
+            "gpu_launches": launches,
+            "clocks": clocks,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

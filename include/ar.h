@@ -1,0 +1,178 @@
+/*
+ * libar: fused N-way partial reduce + residual add + RMSNorm (+ per-token FP8 E4M3)
+ * on one GB300 (sm_103a).
+ *
+ * The N "ranks" of a tensor-parallel all-reduce are N separate device buffers on one
+ * GPU.  The library sums them and, in the fused form, applies the residual add,
+ * RMSNorm (plain or gemma (1 + w) weighting) and an optional dynamic per-token FP8
+ * epilogue, all in one kernel launch on the caller's stream.
+ *
+ * Sources (ROCm/aiter pull-request pages):
+ *   [P1] "[HIP] fix(custom-ar): gfx1250 fused all-reduce + RMSNorm"
+ *   [P2] "[OUTDATED] perf: optimize fused AllReduce + RMSNorm (custom_all_reduce)"
+ *   [P3] "[HIP] [Perf] Specialize partial tiles in two-stage custom all-reduce"
+ *
+ * Numerics (bit-exact with the unfused composition, [P1] Changes; [P2] Technical
+ * Details / 2stage):
+ *   s   = round_T(((float)x_0 + (float)x_1) + ... + (float)x_{N-1})   fp32, rank order
+ *   z   = round_T((float)s + (float)residual_in)                      (z = s if no residual)
+ *   y   = round_T(z * rsqrt(mean_j(z_j^2) + eps) * w'),  w' = w or (1 + w)
+ *   q   = e4m3_satfinite(y / scale), scale = max_j |y_j| / 448     (per row, of the ROUNDED y)
+ * round_T is IEEE round-to-nearest-even.  The sum s and residual_out are bit-exact; y is
+ * within one unit in the last place of the exactly-evaluated formula's rounding; FP8
+ * codes follow from y exactly (IEEE fp32 division, saturating round-to-nearest-even).
+ *
+ * Ownership and side effects: the caller owns every buffer and the stream.  The compute
+ * entry points never allocate, free or synchronise; they validate arguments on the host,
+ * launch exactly one kernel on `stream` (or nothing), and return.  All pointers except
+ * the host array of partial pointers are device pointers; the partial-pointer values
+ * are copied into the kernel parameters, so that array may be reused as soon as the call
+ * returns.  Inputs are not modified (except through the permitted exact aliases).
+ *
+ * Errors: every function returns an ar_status.  Argument errors are detected before
+ * anything is launched and leave all buffers untouched.  AR_ERR_CUDA reports a failed
+ * launch; ar_last_error() gives the CUDA message.  Nothing throws across this ABI.
+ *
+ * Threads: one context may be used by one host thread at a time; distinct contexts
+ * are independent.  A context holds no device memory.
+ */
+#ifndef AR_H
+#define AR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ar_ctx ar_ctx;
+
+typedef enum {
+  AR_OK = 0,
+  AR_ERR_INVALID_ARG = 1,     /* null pointer, n out of range, bad size, dtype, flag or eps */
+  AR_ERR_UNSUPPORTED = 2,     /* device is not sm_103 / feature not available */
+  AR_ERR_ALIGNMENT = 3,       /* a pointer is not aligned to its element size */
+  AR_ERR_CUDA = 4,            /* a CUDA runtime call or kernel launch failed */
+  AR_ERR_NOT_INITIALIZED = 5, /* ctx is NULL */
+  AR_ERR_OVERLAP = 6          /* an output overlaps an input or another output (not an allowed exact alias) */
+} ar_status;
+
+typedef enum { AR_DTYPE_F32 = 0, AR_DTYPE_F16 = 1, AR_DTYPE_BF16 = 2 } ar_dtype;
+
+/* Largest N (number of partial buffers).  TP8 is the widest group on the pages ([P2] Test
+ * Results; [P1] Test results runs TP2/TP4). */
+#define AR_MAX_PARTIALS 8
+
+enum { AR_QUANT_NONE = 0, AR_QUANT_FP8_E4M3_PER_TOKEN = 1 };
+
+/*
+ * Create a context for CUDA device `device` (flags: must be 0).  Queries the SM count,
+ * L2 size and cluster limits once and prepares the kernels (function attributes), so that
+ * later calls can be captured in a CUDA graph.  Counterpart of constructing the
+ * communicator, CustomAllreduce(group, device, max_size) ([P3] bench_allreduce_tail.py
+ * listing).  Returns AR_ERR_UNSUPPORTED on a device other than compute capability 10.3.
+ * The calling thread's current device is left unchanged.
+ */
+ar_status ar_init(ar_ctx** ctx, int device, unsigned flags);
+
+/* Release a context (NULL is accepted).  Counterpart of CustomAllreduce.close() ([P3]). */
+ar_status ar_destroy(ar_ctx* ctx);
+
+/*
+ * Plain sum-reduce of n partials ([P2] Technical Details / 2stage: one thread reduces one
+ * 16-byte pack across all inputs in fp32, in input order, then downcasts once; [P3]
+ * Proposed modifications: full tiles without predicates, leftover packs and elements by
+ * a tail path).  Counterpart of custom_all_reduce(x) / tensor_model_parallel_all_reduce.
+ *
+ *   out[i] = round_T(sum_{r=0..n-1} (float)partials[r][i]) for i in [0, numel)
+ *
+ * out:      device, numel elements of dtype; may equal partials[k] exactly (in place),
+ *           must not overlap any partial otherwise.
+ * partials: HOST array of n device pointers, each numel elements of dtype.
+ * n:        1..AR_MAX_PARTIALS.   numel: >= 0 (0 launches nothing).
+ * dtype:    AR_DTYPE_F32, AR_DTYPE_F16 or AR_DTYPE_BF16 (fp32: the fp32 sum is stored).
+ * stream:   cudaStream_t (NULL = legacy default stream).
+ * Pointers must be aligned to the element size; 16-byte-aligned pointers take the vector
+ * path, others a scalar path with the same results.
+ */
+ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int n, int64_t numel,
+                        ar_dtype dtype, void* stream);
+
+/*
+ * Arguments of the fused call.  All arrays are contiguous row-major; a row is h elements
+ * (padded or strided rows are not part of this contract: [P1] Changes sends them to the
+ * unfused path).  Counterpart of
+ * tensor_model_parallel_fused_allreduce_rmsnorm(x, res, w, eps, gemma_norm=) and of the
+ * unfused rmsnorm2d_fwd_with_add(out, x, res, res_out, w, eps, gemma, 0) ([P1] the
+ * bench_ar_rms.py listing).
+ */
+typedef struct {
+  int n;                                   /* number of partials, 1..AR_MAX_PARTIALS */
+  const void* partials[AR_MAX_PARTIALS];   /* device, [m, h] of dtype each */
+  const void* residual_in;                 /* device [m, h] or NULL (then z = s) */
+  void* residual_out;                      /* device [m, h] or NULL */
+  const void* weight;                      /* device [h] of dtype, required */
+  void* out;                               /* device [m, h]: y (the bf16/fp16 "mirror" when quant is on);
+                                              NULL allowed only when quant is on */
+  float eps;                               /* finite, >= 0 */
+  int gemma;                               /* != 0: weight factor is (1 + w) ([P1] gemma_norm) */
+  int quant;                               /* AR_QUANT_NONE or AR_QUANT_FP8_E4M3_PER_TOKEN */
+  void* q_out;                             /* device [m, h] E4M3 bytes, required when quant is on */
+  float* scale_out;                        /* device [m] fp32 per-row scales, required when quant is on */
+  int64_t m;                               /* rows (tokens), >= 0 (0 launches nothing) */
+  int64_t h;                               /* hidden size, >= 1 */
+  ar_dtype dtype;                          /* AR_DTYPE_BF16 or AR_DTYPE_F16 */
+} ar_fused_args;
+
+/*
+ * Fused reduce + residual add + RMSNorm (+ per-token FP8) in one launch ([P1] Changes:
+ * fixed rank-order accumulation, same bf16/fp16 rounding as the unfused path, gemma_norm,
+ * per-token FP8 output that quantises the rounded output like
+ * dynamic_per_token_scaled_quant, optional bf16 mirror).
+ *
+ * Per row: z and residual_out as in the header comment; y written to `out` if non-NULL;
+ * with quant, scale_out[row] = amax / 448 (fp32) and q_out = e4m3(y / scale), with an
+ * all-zero row giving scale 0 and codes 0.  E4M3 is the OCP "fn" format (max 448).
+ * Aliasing: residual_out and out may each be EXACTLY one of the [m, h] inputs
+ * (residual_in or a partial), because every element is read before the same thread
+ * writes it; any other overlap between an output and an input, or between two outputs,
+ * is refused with AR_ERR_OVERLAP before anything is launched.
+ */
+ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* args, void* stream);
+
+/* Static description of a status code. */
+const char* ar_status_string(ar_status s);
+
+/* The CUDA error text of the last AR_ERR_CUDA on this context ("" if none). */
+const char* ar_last_error(const ar_ctx* ctx);
+
+/* Name of the kernel variant the last successful call launched (tests assert on it):
+ * "reduce_vec", "reduce_vec_tail", "reduce_scalar", "fused_row_vec", "fused_cluster_vec",
+ * "fused_staged", "fused_scalar", "fused_cluster_scalar" or "none" (empty call). */
+const char* ar_last_variant(const ar_ctx* ctx);
+
+/* Tuning and test overrides (0 = automatic for each).  Values outside the documented
+ * range return AR_ERR_INVALID_ARG. */
+typedef enum {
+  AR_OPT_FORCE_VARIANT = 0,  /* 0 auto, 1 row, 2 cluster, 3 staged, 4 scalar (tail) */
+  AR_OPT_CLUSTER_SIZE = 1,   /* 0 auto, else 1, 2, 4, 8 or 16 CTAs per row */
+  AR_OPT_PACKS_PER_THREAD = 2, /* 0 auto, else 1, 2 or 4 16-byte packs per thread */
+  AR_OPT_REDUCE_UNROLL = 3,  /* 0 auto, else 1, 2 or 4 packs per thread per tile */
+  AR_OPT_STAGES = 4          /* 0 auto, else 2..4 shared-memory stages (staged variant) */
+} ar_option;
+ar_status ar_set_option(ar_ctx* ctx, ar_option opt, int64_t value);
+
+/* Read-only facts about the context. */
+typedef enum {
+  AR_INFO_SM_COUNT = 0,
+  AR_INFO_L2_BYTES = 1,
+  AR_INFO_REDUCE_TILE_PACKS = 2, /* 16-byte packs per reduce tile (full-tile unit) */
+  AR_INFO_DEVICE = 3
+} ar_info;
+ar_status ar_get_info(const ar_ctx* ctx, ar_info key, int64_t* value);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AR_H */

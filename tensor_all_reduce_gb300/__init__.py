@@ -1,0 +1,285 @@
+"""Fused N-way partial reduce + residual add + RMSNorm (+ per-token FP8 E4M3) on GB300.
+
+A thin ctypes binding over ``libar.so`` (see ``include/ar.h``).  The functions named like
+the C ABI (``ar_init``, ``ar_reduce_sum``, ``ar_fused_reduce_rmsnorm``, ``ar_destroy`` ...)
+take raw device pointers and sizes exactly as the C functions do; ``reduce_sum`` and
+``fused_reduce_rmsnorm`` marshal torch tensors into those calls.  Every step of the
+computation runs in the library's CUDA kernels: there is no Python or PyTorch compute
+path, and using the package without a built ``libar.so`` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libar.so")
+
+# ---- mirrors of include/ar.h ----------------------------------------------
+AR_OK = 0
+AR_ERR_INVALID_ARG = 1
+AR_ERR_UNSUPPORTED = 2
+AR_ERR_ALIGNMENT = 3
+AR_ERR_CUDA = 4
+AR_ERR_NOT_INITIALIZED = 5
+AR_ERR_OVERLAP = 6
+
+AR_DTYPE_F32 = 0
+AR_DTYPE_F16 = 1
+AR_DTYPE_BF16 = 2
+AR_MAX_PARTIALS = 8
+AR_QUANT_NONE = 0
+AR_QUANT_FP8_E4M3_PER_TOKEN = 1
+
+AR_OPT_FORCE_VARIANT = 0
+AR_OPT_CLUSTER_SIZE = 1
+AR_OPT_PACKS_PER_THREAD = 2
+AR_OPT_REDUCE_UNROLL = 3
+AR_OPT_STAGES = 4
+VARIANT_AUTO, VARIANT_ROW, VARIANT_CLUSTER, VARIANT_STAGED, VARIANT_SCALAR = 0, 1, 2, 3, 4
+
+AR_INFO_SM_COUNT = 0
+AR_INFO_L2_BYTES = 1
+AR_INFO_REDUCE_TILE_PACKS = 2
+AR_INFO_DEVICE = 3
+
+
+class ArFusedArgs(ctypes.Structure):
+    _fields_ = [
+        ("n", ctypes.c_int),
+        ("partials", ctypes.c_void_p * AR_MAX_PARTIALS),
+        ("residual_in", ctypes.c_void_p),
+        ("residual_out", ctypes.c_void_p),
+        ("weight", ctypes.c_void_p),
+        ("out", ctypes.c_void_p),
+        ("eps", ctypes.c_float),
+        ("gemma", ctypes.c_int),
+        ("quant", ctypes.c_int),
+        ("q_out", ctypes.c_void_p),
+        ("scale_out", ctypes.c_void_p),
+        ("m", ctypes.c_int64),
+        ("h", ctypes.c_int64),
+        ("dtype", ctypes.c_int),
+    ]
+
+
+class ArError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str = ""):
+        self.status = status
+        msg = f"{where}: {status_string(status)} ({status})"
+        if detail:
+            msg += f": {detail}"
+        super().__init__(msg)
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libar.so once.  Raises if it has not been built (no fallback exists)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i64, c_int = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.ar_init.argtypes = [ctypes.POINTER(vp), c_int, ctypes.c_uint]
+    lib.ar_destroy.argtypes = [vp]
+    lib.ar_reduce_sum.argtypes = [vp, vp, ctypes.POINTER(vp), c_int, i64, c_int, vp]
+    lib.ar_fused_reduce_rmsnorm.argtypes = [vp, ctypes.POINTER(ArFusedArgs), vp]
+    lib.ar_status_string.argtypes = [c_int]
+    lib.ar_status_string.restype = ctypes.c_char_p
+    lib.ar_last_error.argtypes = [vp]
+    lib.ar_last_error.restype = ctypes.c_char_p
+    lib.ar_last_variant.argtypes = [vp]
+    lib.ar_last_variant.restype = ctypes.c_char_p
+    lib.ar_set_option.argtypes = [vp, c_int, i64]
+    lib.ar_get_info.argtypes = [vp, c_int, ctypes.POINTER(i64)]
+    for f in ("ar_init", "ar_destroy", "ar_reduce_sum", "ar_fused_reduce_rmsnorm", "ar_set_option",
+              "ar_get_info"):
+        getattr(lib, f).restype = c_int
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().ar_status_string(int(status)).decode()
+
+
+# ---- the C ABI, one Python function per entry point -------------------------
+
+def ar_init(device: int = 0, flags: int = 0) -> int:
+    """Create a context; returns its opaque handle (an int)."""
+    lib = load_library()
+    h = ctypes.c_void_p()
+    st = lib.ar_init(ctypes.byref(h), int(device), int(flags))
+    if st != AR_OK:
+        raise ArError(st, "ar_init")
+    return h.value
+
+
+def ar_destroy(ctx: Optional[int]) -> None:
+    st = load_library().ar_destroy(ctx)
+    if st != AR_OK:
+        raise ArError(st, "ar_destroy")
+
+
+def ar_last_variant(ctx: int) -> str:
+    return load_library().ar_last_variant(ctx).decode()
+
+
+def ar_last_error(ctx: int) -> str:
+    return load_library().ar_last_error(ctx).decode()
+
+
+def ar_set_option(ctx: int, opt: int, value: int) -> None:
+    st = load_library().ar_set_option(ctx, int(opt), int(value))
+    if st != AR_OK:
+        raise ArError(st, "ar_set_option")
+
+
+def ar_get_info(ctx: int, key: int) -> int:
+    v = ctypes.c_int64()
+    st = load_library().ar_get_info(ctx, int(key), ctypes.byref(v))
+    if st != AR_OK:
+        raise ArError(st, "ar_get_info")
+    return v.value
+
+
+def _check(ctx, st, where):
+    if st != AR_OK:
+        raise ArError(st, where, ar_last_error(ctx) if (ctx and st == AR_ERR_CUDA) else "")
+
+
+def ar_reduce_sum(ctx: int, out: int, partials: Sequence[int], numel: int, dtype: int,
+                  stream: Optional[int] = None, raise_on_error: bool = True) -> int:
+    """out[i] = round_T(sum_r partials[r][i]).  Pointers are device addresses (ints)."""
+    n = len(partials)
+    arr = (ctypes.c_void_p * max(n, 1))(*partials)
+    st = load_library().ar_reduce_sum(ctx, out, arr, n, int(numel), int(dtype), stream)
+    if raise_on_error:
+        _check(ctx, st, "ar_reduce_sum")
+    return st
+
+
+def ar_fused_reduce_rmsnorm(ctx: int, args: ArFusedArgs, stream: Optional[int] = None,
+                            raise_on_error: bool = True) -> int:
+    st = load_library().ar_fused_reduce_rmsnorm(ctx, ctypes.byref(args), stream)
+    if raise_on_error:
+        _check(ctx, st, "ar_fused_reduce_rmsnorm")
+    return st
+
+
+def make_fused_args(partials: Sequence[int], residual_in: Optional[int], residual_out: Optional[int],
+                    weight: int, out: Optional[int], eps: float, gemma: bool, quant: bool,
+                    q_out: Optional[int], scale_out: Optional[int], m: int, h: int, dtype: int) -> ArFusedArgs:
+    a = ArFusedArgs()
+    a.n = len(partials)
+    for i, p in enumerate(partials):
+        a.partials[i] = p
+    a.residual_in = residual_in
+    a.residual_out = residual_out
+    a.weight = weight
+    a.out = out
+    a.eps = eps
+    a.gemma = int(bool(gemma))
+    a.quant = AR_QUANT_FP8_E4M3_PER_TOKEN if quant else AR_QUANT_NONE
+    a.q_out = q_out
+    a.scale_out = scale_out
+    a.m = m
+    a.h = h
+    a.dtype = dtype
+    return a
+
+
+# ---- torch marshalling -----------------------------------------------------
+
+def _torch_dtype_code(t) -> int:
+    import torch
+    return {torch.float32: AR_DTYPE_F32, torch.float16: AR_DTYPE_F16, torch.bfloat16: AR_DTYPE_BF16}[t.dtype]
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+class Context:
+    """Owns one ar_ctx for a device; torch-tensor front end of the C ABI."""
+
+    def __init__(self, device: int = 0):
+        self.device = device
+        self.handle = ar_init(device)
+
+    def close(self):
+        if self.handle:
+            ar_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def last_variant(self) -> str:
+        return ar_last_variant(self.handle)
+
+    def set_option(self, opt: int, value: int):
+        ar_set_option(self.handle, opt, value)
+
+    def info(self, key: int) -> int:
+        return ar_get_info(self.handle, key)
+
+    def reduce_sum(self, partials, out=None, stream=None):
+        """Sum contiguous same-shaped device tensors in rank order; returns `out`."""
+        import torch
+        x0 = partials[0]
+        for p in partials:
+            if p.shape != x0.shape or p.dtype != x0.dtype or not p.is_contiguous() or not p.is_cuda:
+                raise ValueError("partials must be contiguous CUDA tensors of one shape and dtype")
+        if out is None:
+            out = torch.empty_like(x0)
+        ar_reduce_sum(self.handle, out.data_ptr(), [p.data_ptr() for p in partials], x0.numel(),
+                      _torch_dtype_code(x0), _stream(stream))
+        return out
+
+    def fused_reduce_rmsnorm(self, partials, residual, weight, eps: float = 1e-6, gemma: bool = False,
+                             quant: bool = False, out=None, residual_out=None, q_out=None, scale_out=None,
+                             want_out: bool = True, want_residual_out: bool = True, stream=None):
+        """Returns (out, residual_out, q_out, scale_out); absent outputs are None."""
+        import torch
+        x0 = partials[0]
+        m, h = x0.shape
+        for p in list(partials) + ([residual] if residual is not None else []):
+            if p.shape != (m, h) or p.dtype != x0.dtype or not p.is_contiguous() or not p.is_cuda:
+                raise ValueError("partials and residual must be contiguous [m, h] CUDA tensors of one dtype")
+        if out is None and (want_out or not quant):
+            out = torch.empty_like(x0)
+        if residual_out is None and want_residual_out:
+            residual_out = torch.empty_like(x0)
+        if quant:
+            if q_out is None:
+                q_out = torch.empty((m, h), dtype=torch.uint8, device=x0.device)
+            if scale_out is None:
+                scale_out = torch.empty((m,), dtype=torch.float32, device=x0.device)
+        args = make_fused_args([p.data_ptr() for p in partials], _ptr(residual), _ptr(residual_out),
+                               weight.data_ptr(), _ptr(out), eps, gemma, quant, _ptr(q_out), _ptr(scale_out),
+                               m, h, _torch_dtype_code(x0))
+        ar_fused_reduce_rmsnorm(self.handle, args, _stream(stream))
+        return out, residual_out, q_out, scale_out

@@ -1,0 +1,429 @@
+// C ABI of libar: argument validation, variant selection and the single launch per call.
+//
+// Validation runs before the context is consulted, so argument errors are reported the
+// same way with or without a GPU.  Nothing here allocates device memory, synchronises a
+// stream or blocks: every compute call is one cudaLaunchKernelExC on the caller's stream
+// (or nothing), which keeps the calls capturable in CUDA graphs.
+#include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "ar.h"
+#include "ar_common.cuh"
+#include "ar_launch.h"
+
+struct ar_ctx {
+  int device;
+  int sm_count;
+  int64_t l2_bytes;
+  int max_cluster;       // largest cluster the fused kernel can be launched with
+  // overrides (0 = automatic)
+  int force_variant;
+  int cluster_size;
+  int ppt;
+  int reduce_unroll;
+  int stages;
+  const char* last_variant;
+  char last_error[256];
+};
+
+namespace {
+
+constexpr int kReduceBlock = 256;
+
+// Switch to the context's device for the duration of a call, restoring the caller's.
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) changed = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+int elem_size(ar_dtype d) { return d == AR_DTYPE_F32 ? 4 : 2; }
+
+bool dtype_ok(int d) { return d == AR_DTYPE_F32 || d == AR_DTYPE_F16 || d == AR_DTYPE_BF16; }
+
+uintptr_t addr(const void* p) { return reinterpret_cast<uintptr_t>(p); }
+
+bool overlaps(const void* a, int64_t an, const void* b, int64_t bn) {
+  if (an <= 0 || bn <= 0) return false;
+  return addr(a) < addr(b) + (uintptr_t)bn && addr(b) < addr(a) + (uintptr_t)an;
+}
+
+bool aligned(const void* p, int bytes) { return (addr(p) % (uintptr_t)bytes) == 0; }
+
+ar_status fail_cuda(ar_ctx* ctx, cudaError_t e, const char* what) {
+  if (ctx) snprintf(ctx->last_error, sizeof(ctx->last_error), "%s: %s", what, cudaGetErrorString(e));
+  return AR_ERR_CUDA;
+}
+
+ar_status launch(ar_ctx* ctx, const void* fn, unsigned grid, unsigned block, int csize, void* params,
+                 void* stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid, 1, 1);
+  cfg.blockDim = dim3(block, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  if (csize > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  void* args[1] = {params};
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
+  if (e != cudaSuccess) return fail_cuda(ctx, e, "kernel launch");
+  return AR_OK;
+}
+
+}  // namespace
+
+namespace ar {
+int fused_kernel_list(const void** out, int cap) {
+  int k = 0;
+  for (int dt = 0; dt < 2; ++dt)
+    for (int n = 1; n <= AR_MAX_PARTIALS; ++n)
+      for (int ppt = 1; ppt <= 4; ppt *= 2)
+        for (int q = 0; q < 2; ++q)
+          for (int v = 0; v < 2; ++v) {
+            if (!v && ppt != 1) continue;  // the scalar form has one pack per thread
+            const void* fn = dt ? fused_kernel_bf16(n, ppt, q != 0, v != 0) : fused_kernel_f16(n, ppt, q != 0, v != 0);
+            if (fn && k < cap) out[k++] = fn;
+          }
+  return k;
+}
+}  // namespace ar
+
+extern "C" {
+
+const char* ar_status_string(ar_status s) {
+  switch (s) {
+    case AR_OK: return "success";
+    case AR_ERR_INVALID_ARG: return "invalid argument";
+    case AR_ERR_UNSUPPORTED: return "unsupported device or configuration";
+    case AR_ERR_ALIGNMENT: return "pointer not aligned to its element size";
+    case AR_ERR_CUDA: return "CUDA error";
+    case AR_ERR_NOT_INITIALIZED: return "context not initialised";
+    case AR_ERR_OVERLAP: return "output overlaps an input or another output";
+  }
+  return "unknown status";
+}
+
+const char* ar_last_error(const ar_ctx* ctx) { return ctx ? ctx->last_error : ""; }
+
+const char* ar_last_variant(const ar_ctx* ctx) { return ctx ? ctx->last_variant : ""; }
+
+ar_status ar_init(ar_ctx** out, int device, unsigned flags) {
+  if (!out) return AR_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (flags != 0) return AR_ERR_INVALID_ARG;
+  int count = 0;
+  cudaError_t e = cudaGetDeviceCount(&count);
+  if (e != cudaSuccess) return AR_ERR_CUDA;
+  if (device < 0 || device >= count) return AR_ERR_INVALID_ARG;
+  int major = 0, minor = 0, sms = 0, l2 = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, device) != cudaSuccess)
+    return AR_ERR_CUDA;
+  if (major != 10 || minor != 3) return AR_ERR_UNSUPPORTED;  // built for sm_103a only
+
+  ar_ctx* ctx = static_cast<ar_ctx*>(calloc(1, sizeof(ar_ctx)));
+  if (!ctx) return AR_ERR_INVALID_ARG;
+  ctx->device = device;
+  ctx->sm_count = sms;
+  ctx->l2_bytes = l2;
+  ctx->last_variant = "none";
+  ctx->max_cluster = 8;
+
+  DeviceGuard g(device);
+  // Load every kernel now (lazy module loading would otherwise do it on first launch,
+  // possibly inside a stream capture) and allow 16-CTA clusters for the fused kernels.
+  const void* fns[512];
+  int nf = ar::fused_kernel_list(fns, 512);
+  for (int i = 0; i < nf; ++i) {
+    e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) {
+      free(ctx);
+      return AR_ERR_CUDA;
+    }
+  }
+  for (int dt = 0; dt < 3; ++dt)
+    for (int n = 1; n <= AR_MAX_PARTIALS; ++n)
+      for (int u = 1; u <= 4; u += 3)
+        for (int v = 0; v < 2; ++v)
+          for (int t = 0; t < 2; ++t) {
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, ar::reduce_kernel(dt, n, u, v != 0, t != 0));
+            if (e != cudaSuccess) {
+              free(ctx);
+              return AR_ERR_CUDA;
+            }
+          }
+  // Largest cluster the fused kernel supports with a small block on this device.
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16, 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int csz = 0;
+    if (cudaOccupancyMaxPotentialClusterSize(&csz, ar::fused_kernel_bf16(4, 1, true, true), &cfg) ==
+            cudaSuccess &&
+        csz >= 1)
+      ctx->max_cluster = csz >= 16 ? 16 : (csz >= 8 ? 8 : (csz >= 4 ? 4 : (csz >= 2 ? 2 : 1)));
+    cudaGetLastError();
+  }
+  *out = ctx;
+  return AR_OK;
+}
+
+ar_status ar_destroy(ar_ctx* ctx) {
+  free(ctx);
+  return AR_OK;
+}
+
+ar_status ar_set_option(ar_ctx* ctx, ar_option opt, int64_t v) {
+  if (!ctx) return AR_ERR_NOT_INITIALIZED;
+  switch (opt) {
+    case AR_OPT_FORCE_VARIANT:
+      if (v < 0 || v > 4) return AR_ERR_INVALID_ARG;
+      ctx->force_variant = (int)v;
+      return AR_OK;
+    case AR_OPT_CLUSTER_SIZE:
+      if (!(v == 0 || v == 1 || v == 2 || v == 4 || v == 8 || v == 16)) return AR_ERR_INVALID_ARG;
+      ctx->cluster_size = (int)v;
+      return AR_OK;
+    case AR_OPT_PACKS_PER_THREAD:
+      if (!(v == 0 || v == 1 || v == 2 || v == 4)) return AR_ERR_INVALID_ARG;
+      ctx->ppt = (int)v;
+      return AR_OK;
+    case AR_OPT_REDUCE_UNROLL:
+      if (!(v == 0 || v == 1 || v == 4)) return AR_ERR_INVALID_ARG;
+      ctx->reduce_unroll = (int)v;
+      return AR_OK;
+    case AR_OPT_STAGES:
+      if (!(v == 0 || (v >= 2 && v <= 4))) return AR_ERR_INVALID_ARG;
+      ctx->stages = (int)v;
+      return AR_OK;
+  }
+  return AR_ERR_INVALID_ARG;
+}
+
+ar_status ar_get_info(const ar_ctx* ctx, ar_info key, int64_t* value) {
+  if (!value) return AR_ERR_INVALID_ARG;
+  if (!ctx) return AR_ERR_NOT_INITIALIZED;
+  switch (key) {
+    case AR_INFO_SM_COUNT: *value = ctx->sm_count; return AR_OK;
+    case AR_INFO_L2_BYTES: *value = ctx->l2_bytes; return AR_OK;
+    case AR_INFO_REDUCE_TILE_PACKS:
+      *value = (int64_t)kReduceBlock * (ctx->reduce_unroll ? ctx->reduce_unroll : 4);
+      return AR_OK;
+    case AR_INFO_DEVICE: *value = ctx->device; return AR_OK;
+  }
+  return AR_ERR_INVALID_ARG;
+}
+
+// ---------------------------------------------------------------------------
+// plain reduce
+// ---------------------------------------------------------------------------
+
+ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int n, int64_t numel,
+                        ar_dtype dtype, void* stream) {
+  if (!out || !partials || n < 1 || n > AR_MAX_PARTIALS || numel < 0 || !dtype_ok(dtype))
+    return AR_ERR_INVALID_ARG;
+  const int es = elem_size(dtype);
+  if (numel > INT64_MAX / 16) return AR_ERR_INVALID_ARG;
+  const int64_t bytes = numel * es;
+  if (!aligned(out, es)) return AR_ERR_ALIGNMENT;
+  for (int r = 0; r < n; ++r) {
+    if (!partials[r]) return AR_ERR_INVALID_ARG;
+    if (!aligned(partials[r], es)) return AR_ERR_ALIGNMENT;
+    if (partials[r] != out && overlaps(out, bytes, partials[r], bytes)) return AR_ERR_OVERLAP;
+  }
+  if (!ctx) return AR_ERR_NOT_INITIALIZED;
+  if (numel == 0) {
+    ctx->last_variant = "none";
+    return AR_OK;
+  }
+
+  ar::ReduceParams p;
+  memset(&p, 0, sizeof(p));
+  for (int r = 0; r < n; ++r) p.x[r] = partials[r];
+  p.out = out;
+  p.numel = numel;
+  bool vec = aligned(out, 16);
+  for (int r = 0; r < n; ++r) vec = vec && aligned(partials[r], 16);
+  if (ctx->force_variant == 4) vec = false;
+
+  DeviceGuard g(ctx->device);
+  const int max_grid = ctx->sm_count * (2048 / kReduceBlock);
+  unsigned grid;
+  const void* fn;
+  const char* name;
+  if (vec) {
+    const int epp = 16 / es;
+    p.npacks = numel / epp;
+    int unroll = ctx->reduce_unroll;
+    if (unroll == 0) unroll = (p.npacks >= (int64_t)max_grid * kReduceBlock * 4) ? 4 : 1;
+    const int64_t tile = (int64_t)kReduceBlock * unroll;
+    p.full_tiles = p.npacks / tile;
+    const bool has_tail = (p.npacks % tile) != 0 || (numel % epp) != 0;
+    int64_t gr = p.full_tiles < max_grid ? p.full_tiles : max_grid;
+    if (gr < 1) gr = 1;
+    grid = (unsigned)gr;
+    fn = ar::reduce_kernel(dtype, n, unroll, true, has_tail);
+    name = has_tail ? "reduce_vec_tail" : "reduce_vec";
+  } else {
+    int64_t gr = (numel + kReduceBlock - 1) / kReduceBlock;
+    if (gr > max_grid) gr = max_grid;
+    grid = (unsigned)gr;
+    fn = ar::reduce_kernel(dtype, n, 1, false, false);
+    name = "reduce_scalar";
+  }
+  if (!fn) return AR_ERR_UNSUPPORTED;
+  ar_status st = launch(ctx, fn, grid, kReduceBlock, 1, &p, stream);
+  if (st == AR_OK) ctx->last_variant = name;
+  return st;
+}
+
+// ---------------------------------------------------------------------------
+// fused reduce + residual + RMSNorm (+ FP8)
+// ---------------------------------------------------------------------------
+
+ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* stream) {
+  if (!a) return AR_ERR_INVALID_ARG;
+  if (a->n < 1 || a->n > AR_MAX_PARTIALS || a->m < 0 || a->h < 1 || !a->weight) return AR_ERR_INVALID_ARG;
+  if (a->dtype != AR_DTYPE_BF16 && a->dtype != AR_DTYPE_F16) return AR_ERR_INVALID_ARG;
+  if (a->quant != AR_QUANT_NONE && a->quant != AR_QUANT_FP8_E4M3_PER_TOKEN) return AR_ERR_INVALID_ARG;
+  const bool quant = a->quant == AR_QUANT_FP8_E4M3_PER_TOKEN;
+  if (quant && (!a->q_out || !a->scale_out)) return AR_ERR_INVALID_ARG;
+  if (!quant && !a->out) return AR_ERR_INVALID_ARG;
+  if (!(a->eps >= 0.0f) || isinf(a->eps)) return AR_ERR_INVALID_ARG;  // also rejects NaN
+  if (a->h > (int64_t)1 << 30 || a->m > ((int64_t)1 << 40) / a->h) return AR_ERR_INVALID_ARG;
+  for (int r = 0; r < a->n; ++r)
+    if (!a->partials[r]) return AR_ERR_INVALID_ARG;
+
+  const int es = elem_size(a->dtype);
+  const int64_t mh = a->m * a->h;
+  const int64_t tb = mh * es;  // bytes of one [m, h] tensor
+  // element alignment
+  for (int r = 0; r < a->n; ++r)
+    if (!aligned(a->partials[r], es)) return AR_ERR_ALIGNMENT;
+  if ((a->residual_in && !aligned(a->residual_in, es)) || (a->residual_out && !aligned(a->residual_out, es)) ||
+      !aligned(a->weight, es) || (a->out && !aligned(a->out, es)) || (quant && !aligned(a->scale_out, 4)))
+    return AR_ERR_ALIGNMENT;
+  // overlap: outputs may equal an [m, h] input of the same type exactly (every element is
+  // read before the same thread writes it), never partially overlap an input, and never
+  // overlap one another
+  struct Range { const void* p; int64_t n; bool same_shape; };
+  Range ins[AR_MAX_PARTIALS + 2];
+  int ni = 0;
+  for (int r = 0; r < a->n; ++r) ins[ni++] = {a->partials[r], tb, true};
+  if (a->residual_in) ins[ni++] = {a->residual_in, tb, true};
+  ins[ni++] = {a->weight, (int64_t)a->h * es, false};
+  Range outs[4];
+  int no = 0;
+  if (a->residual_out) outs[no++] = {a->residual_out, tb, true};
+  if (a->out) outs[no++] = {a->out, tb, true};
+  if (quant) {
+    outs[no++] = {a->q_out, mh, false};
+    outs[no++] = {a->scale_out, a->m * 4, false};
+  }
+  for (int o = 0; o < no; ++o) {
+    for (int i = 0; i < ni; ++i) {
+      if (outs[o].same_shape && ins[i].same_shape && outs[o].p == ins[i].p) continue;
+      if (overlaps(outs[o].p, outs[o].n, ins[i].p, ins[i].n)) return AR_ERR_OVERLAP;
+    }
+    for (int o2 = o + 1; o2 < no; ++o2)
+      if (overlaps(outs[o].p, outs[o].n, outs[o2].p, outs[o2].n)) return AR_ERR_OVERLAP;
+  }
+  if (!ctx) return AR_ERR_NOT_INITIALIZED;
+  if (a->m == 0) {
+    ctx->last_variant = "none";
+    return AR_OK;
+  }
+
+  // ---- variant selection ----
+  bool vec = (a->h % 8) == 0;
+  for (int r = 0; r < a->n; ++r) vec = vec && aligned(a->partials[r], 16);
+  vec = vec && (!a->residual_in || aligned(a->residual_in, 16)) && (!a->residual_out || aligned(a->residual_out, 16)) &&
+        aligned(a->weight, 16) && (!a->out || aligned(a->out, 16)) && (!quant || aligned(a->q_out, 8));
+  if (ctx->force_variant == 4) vec = false;
+
+  const int row_packs = (int)((a->h + 7) / 8);
+  const int max_cl = ctx->max_cluster;
+  int csize;
+  if (ctx->cluster_size) {
+    csize = ctx->cluster_size;
+  } else if (ctx->force_variant == 1) {
+    csize = 1;
+  } else {
+    // spread small batches over the SMs: grow the cluster while fewer than two CTAs per
+    // SM would be launched and every CTA keeps at least 32 packs (256 elements)
+    csize = 1;
+    const int64_t target = 2LL * ctx->sm_count;
+    while (csize < max_cl && a->m * csize < target && row_packs / (csize * 2) >= 32) csize *= 2;
+    if (ctx->force_variant == 2 && csize == 1) csize = 2;
+  }
+  // a CTA holds at most 1024 packs (1024 / ppt threads of ppt packs, the kernels' launch
+  // bound): widen the cluster for very long rows
+  constexpr int kMaxPacksPerCta = 1024;
+  while (csize < max_cl && (row_packs + csize - 1) / csize > kMaxPacksPerCta) csize *= 2;
+  if (csize > max_cl) csize = max_cl;
+  const int chunk = (row_packs + csize - 1) / csize;
+  if (chunk > kMaxPacksPerCta) return AR_ERR_UNSUPPORTED;  // h > 8192 * max cluster size
+  int ppt = vec ? ctx->ppt : 1;
+  if (ppt == 0) ppt = chunk <= 256 ? 1 : 2;
+  int block = ((chunk + ppt - 1) / ppt + 31) / 32 * 32;
+  if (block < 32) block = 32;
+  const int64_t grid = a->m * csize;
+  if (grid > 0x7FFFFFFFLL) return AR_ERR_UNSUPPORTED;
+
+  ar::FusedParams p;
+  memset(&p, 0, sizeof(p));
+  for (int r = 0; r < a->n; ++r) p.x[r] = a->partials[r];
+  p.res_in = a->residual_in;
+  p.res_out = a->residual_out;
+  p.w = a->weight;
+  p.out = a->out;
+  p.q = static_cast<uint8_t*>(a->q_out);
+  p.scale = a->scale_out;
+  p.m = a->m;
+  p.h = (int)a->h;
+  p.row_packs = row_packs;
+  p.chunk_packs = chunk;
+  p.csize = csize;
+  p.eps = a->eps;
+  p.inv_h = (float)(1.0 / (double)a->h);
+  p.gemma = a->gemma != 0;
+
+  const void* fn = a->dtype == AR_DTYPE_BF16 ? ar::fused_kernel_bf16(a->n, ppt, quant, vec)
+                                             : ar::fused_kernel_f16(a->n, ppt, quant, vec);
+  if (!fn) return AR_ERR_UNSUPPORTED;
+  DeviceGuard g(ctx->device);
+  ar_status st = launch(ctx, fn, (unsigned)grid, (unsigned)block, csize, &p, stream);
+  if (st == AR_OK) {
+    if (vec)
+      ctx->last_variant = csize > 1 ? "fused_cluster_vec" : "fused_row_vec";
+    else
+      ctx->last_variant = csize > 1 ? "fused_cluster_scalar" : "fused_scalar";
+  }
+  return st;
+}
+
+}  // extern "C"

@@ -1,0 +1,261 @@
+// Device building blocks shared by the libar kernels (sm_103a).
+//
+// A "pack" is 16 bytes: 8 bf16/fp16 or 4 fp32 elements, the unit of every vector load and
+// store (page "[OUTDATED] perf: optimize fused AllReduce + RMSNorm (custom_all_reduce)",
+// Technical Details / 2stage: each thread reduces one 16-byte pack across all inputs).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ar {
+
+enum DType : int { kF32 = 0, kF16 = 1, kBF16 = 2 };
+
+constexpr int kMaxPartials = 8;
+constexpr int kPackBytes = 16;
+
+// ---------------------------------------------------------------------------
+// kernel parameter blocks (passed by value; the partial pointers travel in them)
+// ---------------------------------------------------------------------------
+struct ReduceParams {
+  const void* x[kMaxPartials];
+  void* out;
+  int64_t npacks;      // full 16-byte packs
+  int64_t numel;       // elements
+  int64_t full_tiles;  // npacks / (blockDim * unroll)
+};
+
+struct FusedParams {
+  const void* x[kMaxPartials];
+  const void* res_in;
+  void* res_out;
+  const void* w;
+  void* out;
+  uint8_t* q;
+  float* scale;
+  int64_t m;
+  int h;             // elements per row
+  int row_packs;     // packs (8 elements) per row, ceil(h / 8)
+  int chunk_packs;   // packs per CTA of a cluster (== row_packs without a cluster)
+  int csize;         // CTAs per row (cluster size), 1..16
+  float eps;
+  float inv_h;       // 1 / h
+  int gemma;
+};
+
+// ---------------------------------------------------------------------------
+// memory access
+// ---------------------------------------------------------------------------
+
+// 16-byte streaming load through the non-coherent path without L1 allocation: every
+// input element is read exactly once per call.
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+// 16-byte load kept in L1/L2 normally (the weight row, re-read by every row's CTA).
+__device__ __forceinline__ uint4 ld_keep(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint16_t ld_u16(const void* p) {
+  unsigned short v;
+  asm("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ float ld_f32(const void* p) {
+  float v;
+  asm("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_v4(void* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_v2(void* p, uint2 v) {
+  asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void st_u16(void* p, uint16_t v) {
+  asm volatile("st.global.u16 [%0], %1;" ::"l"(p), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_u8(void* p, uint8_t v) {
+  asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "h"((unsigned short)v) : "memory");
+}
+
+__device__ __forceinline__ void st_f32(void* p, float v) {
+  asm volatile("st.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// element conversions (hardware cvt, round-to-nearest-even)
+// ---------------------------------------------------------------------------
+
+template <int DT>
+__device__ __forceinline__ float to_f32(uint32_t bits16);
+
+template <>
+__device__ __forceinline__ float to_f32<kBF16>(uint32_t b) {
+  return __uint_as_float(b << 16);
+}
+
+template <>
+__device__ __forceinline__ float to_f32<kF16>(uint32_t b) {
+  float f;
+  unsigned short h = (unsigned short)b;
+  asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+  return f;
+}
+
+// Round two floats to the 16-bit type and pack them: `lo` in bits 0..15.
+template <int DT>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi);
+
+template <>
+__device__ __forceinline__ uint32_t pack2<kBF16>(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <>
+__device__ __forceinline__ uint32_t pack2<kF16>(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <int DT>
+__device__ __forceinline__ uint16_t round1(float v) {
+  return (uint16_t)(pack2<DT>(v, 0.0f) & 0xFFFFu);
+}
+
+// Unpack the 8 16-bit elements of a pack into floats (element 0 = lowest address).
+template <int DT>
+__device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = to_f32<DT>(w[i] & 0xFFFFu);
+    f[2 * i + 1] = to_f32<DT>(w[i] >> 16);
+  }
+}
+
+template <int DT>
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint4 v;
+  v.x = pack2<DT>(f[0], f[1]);
+  v.y = pack2<DT>(f[2], f[3]);
+  v.z = pack2<DT>(f[4], f[5]);
+  v.w = pack2<DT>(f[6], f[7]);
+  return v;
+}
+
+// Two fp32 values -> two OCP E4M3 codes, saturating to +-448, round-to-nearest-even;
+// `lo` goes to bits 0..7.
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  unsigned short r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// reductions
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Block-wide sum (MAX=false) or max (MAX=true) returned to every thread.  `buf` holds one
+// float per warp and must not be reused by another reduction before a __syncthreads.
+// Warp totals are combined in warp order, so every thread sees the same value.
+template <bool MAX>
+__device__ __forceinline__ float block_allreduce(float v, float* buf) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  v = MAX ? warp_max(v) : warp_sum(v);
+  if (lane == 0) buf[warp] = v;
+  __syncthreads();
+  float t = buf[0];
+  for (int i = 1; i < nwarps; ++i) t = MAX ? fmaxf(t, buf[i]) : t + buf[i];
+  return t;
+}
+
+// ---------------------------------------------------------------------------
+// thread-block clusters: one row split over csize CTAs, partial results exchanged
+// through distributed shared memory (no multicast)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+  cluster_arrive();
+  cluster_wait();
+}
+
+// Read a float from the shared memory of CTA `rank` of this cluster at the address that
+// `local` has in this CTA.
+__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
+  uint32_t a = (uint32_t)__cvta_generic_to_shared(local), ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+  return v;
+}
+
+// Combine one value per CTA over the cluster; every thread of every CTA gets the same
+// result.  `slot` is this CTA's published value (written by thread 0 before the call),
+// `bcast` a one-float broadcast cell.  Starts with a full cluster barrier so every slot is
+// written and visible.  The caller must not let a CTA exit while a peer may still read
+// its slot: after the last exchange it executes cluster_arrive(), and cluster_wait()
+// before returning.  Slots must not be rewritten between exchanges.
+template <bool MAX>
+__device__ __forceinline__ float cluster_gather(const float* slot, float* bcast, int csize) {
+  cluster_sync();
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    float v = 0.0f;  // identity for the sum, and for the max of magnitudes
+    if (lane < csize) v = ld_dsmem(slot, (uint32_t)lane);
+    v = MAX ? warp_max(v) : warp_sum(v);
+    if (lane == 0) *bcast = v;
+  }
+  __syncthreads();
+  return *bcast;
+}
+
+}  // namespace ar

@@ -1,0 +1,209 @@
+// Fused N-way reduce + residual add + RMSNorm (+ per-token FP8 E4M3) kernel.
+//
+// Semantics (page "[HIP] fix(custom-ar): gfx1250 fused all-reduce + RMSNorm", Changes):
+// ranks are summed in fixed order in fp32 and rounded once to the storage type, the
+// residual is added and rounded again exactly as the unfused rmsnorm2d_fwd_with_add
+// does, the row is normalised (plain or gemma (1 + w) weight), and the optional FP8
+// epilogue quantises the ROUNDED output per row with the steps of
+// dynamic_per_token_scaled_quant, writing the 16-bit mirror as well.
+//
+// Work decomposition (GB300 design, not the pages'): a row of h elements is split over a
+// thread-block cluster of `csize` CTAs (csize = 1: one CTA per row).  Each CTA owns a
+// contiguous chunk of 16-byte packs; each thread owns PPT packs strided by blockDim.
+// The row's square-sum and, with FP8, its amax are combined warp -> block (shared
+// memory) -> cluster (distributed shared memory).  Small-M decode shapes use csize > 1 so
+// that the few rows still spread over many SMs; large M uses csize = 1.
+//
+// VEC = true : every pack is a full, 16-byte-aligned group of 8 elements (h % 8 == 0 and
+//              all row starts aligned); one 128-bit load per pack and partial.
+// VEC = false: the tail specialisation for rows whose length is not a multiple of the
+//              pack or whose pointers are not 16-byte aligned: the same packs of 8
+//              elements, loaded element by element with a per-element predicate
+//              (page "[HIP] [Perf] Specialize partial tiles in two-stage custom
+//              all-reduce", Proposed modifications: leftover elements take a predicated
+//              path; no barrier ever sits inside a loop whose trip count differs
+//              between threads).
+#pragma once
+
+#include "ar_common.cuh"
+
+namespace ar {
+
+// Load one pack (8 elements starting at element index e0 of `base`) as floats.
+// Elements at or beyond `limit` (scalar variant only) read as 0.
+template <int DT, bool VEC, bool STREAM>
+__device__ __forceinline__ void load_pack(const void* base, int64_t e0, int64_t limit, float (&f)[8]) {
+  const uint16_t* b = static_cast<const uint16_t*>(base);
+  if constexpr (VEC) {
+    uint4 v = STREAM ? ld_stream(b + e0) : ld_keep(b + e0);
+    unpack8<DT>(v, f);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = (e0 + i < limit) ? to_f32<DT>(ld_u16(b + e0 + i)) : 0.0f;
+  }
+}
+
+// Store one pack of 16-bit values (already rounded, packed in a uint4).
+template <bool VEC>
+__device__ __forceinline__ void store_pack(void* base, int64_t e0, int64_t limit, const uint4& v) {
+  uint16_t* b = static_cast<uint16_t*>(base);
+  if constexpr (VEC) {
+    st_v4(b + e0, v);
+  } else {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (e0 + i < limit) st_u16(b + e0 + i, (uint16_t)((w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu));
+  }
+}
+
+template <int DT, int N, int PPT, bool QUANT, bool VEC>
+__global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) {
+  __shared__ float red_ss[32];
+  __shared__ float red_amax[32];
+  __shared__ float slot_ss, slot_amax, bcast;
+
+  const int csize = p.csize;
+  const int crank = (int)(blockIdx.x % (unsigned)csize);  // == %cluster_ctarank for (csize,1,1) clusters
+  const int64_t row = blockIdx.x / (unsigned)csize;
+  const int pk_begin = crank * p.chunk_packs;
+  const int pk_end = min(pk_begin + p.chunk_packs, p.row_packs);
+  const int64_t row_e = row * (int64_t)p.h;   // first element of the row
+  const int64_t row_end = row_e + p.h;         // one past the row's last element
+
+  // ---- phase 1: loads of every pack this thread owns, then the reduction --------------
+  // Indices of packs beyond the chunk are clamped to the chunk's first pack so that all
+  // loads are unconditional and can be issued back to back; their results are discarded.
+  uint4 z[PPT];
+  uint4 wpk[PPT];
+  bool valid[PPT];
+  float ss = 0.0f;
+#pragma unroll
+  for (int k = 0; k < PPT; ++k) {
+    const int pk = pk_begin + (int)threadIdx.x + k * (int)blockDim.x;
+    valid[k] = pk < pk_end;
+    const int pkc = valid[k] ? pk : pk_begin;
+    const int64_t e0 = row_e + (int64_t)pkc * 8;
+    const int64_t lim = valid[k] ? row_end : row_e;  // scalar variant: nothing for clamped packs
+    float acc[8];
+    load_pack<DT, VEC, true>(p.x[0], e0, lim, acc);
+#pragma unroll
+    for (int r = 1; r < N; ++r) {
+      float t[8];
+      load_pack<DT, VEC, true>(p.x[r], e0, lim, t);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = acc[i] + t[i];  // fp32, rank order 0..N-1
+    }
+    uint4 s = pack8<DT>(acc);                              // one rounding to T
+    if (p.res_in != nullptr) {
+      float sf[8], rf[8];
+      unpack8<DT>(s, sf);
+      load_pack<DT, VEC, true>(p.res_in, e0, lim, rf);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sf[i] = sf[i] + rf[i];
+      s = pack8<DT>(sf);                                   // second rounding to T
+    }
+    z[k] = s;
+    // weight row: 8 consecutive entries starting at column pkc * 8
+    {
+      float wf[8];
+      const int64_t c0 = (int64_t)pkc * 8;
+      load_pack<DT, VEC, false>(p.w, c0, valid[k] ? (int64_t)p.h : 0, wf);
+      wpk[k] = pack8<DT>(wf);                              // exact: wf are T values
+    }
+    if (valid[k]) {
+      float zf[8];
+      unpack8<DT>(z[k], zf);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ss = fmaf(zf[i], zf[i], ss);  // absent elements are 0
+    }
+  }
+  if (p.res_out != nullptr) {
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+      if (valid[k]) {
+        const int pk = pk_begin + (int)threadIdx.x + k * (int)blockDim.x;
+        store_pack<VEC>(p.res_out, row_e + (int64_t)pk * 8, row_end, z[k]);
+      }
+    }
+  }
+
+  // ---- row square-sum: warp -> block -> cluster ------------------------------------
+  float tot = block_allreduce<false>(ss, red_ss);
+  if (csize > 1) {
+    if (threadIdx.x == 0) slot_ss = tot;
+    tot = cluster_gather<false>(&slot_ss, &bcast, csize);
+  }
+  const float inv = rsqrtf(tot * p.inv_h + p.eps);
+
+  // ---- phase 2: normalise, weight, round ---------------------------------------------
+  uint4 y[PPT];
+  float amax = 0.0f;
+#pragma unroll
+  for (int k = 0; k < PPT; ++k) {
+    float zf[8], wf[8], yf[8];
+    unpack8<DT>(z[k], zf);
+    unpack8<DT>(wpk[k], wf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float wv = p.gemma ? 1.0f + wf[i] : wf[i];
+      yf[i] = (zf[i] * inv) * wv;
+    }
+    y[k] = pack8<DT>(yf);
+    if (QUANT && valid[k]) {
+      float yr[8];
+      unpack8<DT>(y[k], yr);                               // amax of the ROUNDED output
+#pragma unroll
+      for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(yr[i]));
+    }
+  }
+  if (p.out != nullptr) {
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+      if (valid[k]) {
+        const int pk = pk_begin + (int)threadIdx.x + k * (int)blockDim.x;
+        store_pack<VEC>(p.out, row_e + (int64_t)pk * 8, row_end, y[k]);
+      }
+    }
+  }
+
+  // ---- FP8 epilogue ----------------------------------------------------------------
+  if constexpr (QUANT) {
+    float am = block_allreduce<true>(amax, red_amax);
+    if (csize > 1) {
+      if (threadIdx.x == 0) slot_amax = am;
+      am = cluster_gather<true>(&slot_amax, &bcast, csize);
+    }
+    const float scale = __fdiv_rn(am, 448.0f);
+    if (crank == 0 && threadIdx.x == 0) st_f32(p.scale + row, scale);
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+      if (!valid[k]) continue;
+      const int pk = pk_begin + (int)threadIdx.x + k * (int)blockDim.x;
+      float yr[8];
+      unpack8<DT>(y[k], yr);
+      uint32_t c[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = am == 0.0f ? 0.0f : __fdiv_rn(yr[2 * i], scale);
+        const float b = am == 0.0f ? 0.0f : __fdiv_rn(yr[2 * i + 1], scale);
+        c[i] = e4m3x2(a, b);
+      }
+      const int64_t e0 = row_e + (int64_t)pk * 8;
+      if constexpr (VEC) {
+        st_v2(p.q + e0, make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16)));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (e0 + i < row_end) st_u8(p.q + e0 + i, (uint8_t)((c[i >> 1] >> (8 * (i & 1))) & 0xFFu));
+      }
+    }
+  }
+
+  if (csize > 1) {
+    cluster_arrive();  // done reading peers' slots
+    cluster_wait();    // and no peer still reads ours
+  }
+}
+
+}  // namespace ar

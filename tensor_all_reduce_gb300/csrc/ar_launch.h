@@ -1,0 +1,20 @@
+// Internal interface between the C-ABI layer and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace ar {
+
+// Kernel entry for a plain reduce: dtype (kF32/kF16/kBF16), n in 1..8, unroll 1 or 4,
+// vec = 16-byte path (else element-wise), has_tail = leftover packs/elements exist.
+const void* reduce_kernel(int dtype, int n, int unroll, bool vec, bool has_tail);
+
+// Kernel entry for the fused path: dtype kF16/kBF16, n in 1..8, ppt 1/2/4 packs per
+// thread (vec only; the scalar tail form has ppt 1), quant = FP8 epilogue.
+const void* fused_kernel_f16(int n, int ppt, bool quant, bool vec);
+const void* fused_kernel_bf16(int n, int ppt, bool quant, bool vec);
+
+// Every fused kernel entry, for one-time attribute setup (non-portable cluster sizes).
+int fused_kernel_list(const void** out, int cap);
+
+}  // namespace ar

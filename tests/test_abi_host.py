@@ -1,0 +1,136 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports every entry
+point include/ar.h declares, and rejects bad arguments before launching anything.
+
+Argument validation runs before the context is consulted, so with ctx = NULL a bad call
+returns its argument error and a good call returns AR_ERR_NOT_INITIALIZED.  Pointer values
+below are never dereferenced (they are only compared and range-checked on the host).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import tensor_all_reduce_gb300 as tar
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ar.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from tensor_all_reduce_gb300 import _build
+    _build.build()
+    return tar.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:ar_status|const char\s*\*)\s*(ar_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("ar_init", "ar_reduce_sum", "ar_fused_reduce_rmsnorm", "ar_destroy", "ar_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, f"not exported: {missing}"
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert tar.status_string(code) not in ("", "unknown status")
+    assert tar.status_string(99) == "unknown status"
+
+
+def test_null_context_queries(lib):
+    v = ctypes.c_int64()
+    assert lib.ar_get_info(None, tar.AR_INFO_SM_COUNT, ctypes.byref(v)) == tar.AR_ERR_NOT_INITIALIZED
+    assert lib.ar_set_option(None, tar.AR_OPT_CLUSTER_SIZE, 4) == tar.AR_ERR_NOT_INITIALIZED
+    assert lib.ar_destroy(None) == tar.AR_OK
+    assert tar.ar_last_variant(None) == ""
+    assert lib.ar_init(None, 0, 0) == tar.AR_ERR_INVALID_ARG
+
+
+BASE = 1 << 40   # fake, well-aligned device addresses; never dereferenced
+MB = 1 << 20
+
+
+def reduce_status(out, parts, numel, dtype=tar.AR_DTYPE_BF16):
+    return tar.ar_reduce_sum(None, out, parts, numel, dtype, None, raise_on_error=False)
+
+
+def test_reduce_validation(lib):
+    p = [BASE + i * MB for i in range(4)]
+    out = BASE + 16 * MB
+    assert reduce_status(out, p, 1000) == tar.AR_ERR_NOT_INITIALIZED           # valid
+    assert reduce_status(p[2], p, 1000) == tar.AR_ERR_NOT_INITIALIZED          # exact in-place alias
+    assert reduce_status(0, p, 1000) == tar.AR_ERR_INVALID_ARG                 # null out
+    assert reduce_status(out, [], 1000) == tar.AR_ERR_INVALID_ARG              # n = 0
+    assert reduce_status(out, p * 3, 1000) == tar.AR_ERR_INVALID_ARG           # n = 12 > 8
+    assert reduce_status(out, p, -1) == tar.AR_ERR_INVALID_ARG                 # negative numel
+    assert reduce_status(out, p, 10, dtype=7) == tar.AR_ERR_INVALID_ARG        # bad dtype
+    assert reduce_status(out, p[:1] + [0], 10) == tar.AR_ERR_INVALID_ARG       # null partial
+    assert reduce_status(out + 1, p, 10) == tar.AR_ERR_ALIGNMENT               # odd address, bf16
+    assert reduce_status(out + 2, p, 10, tar.AR_DTYPE_F32) == tar.AR_ERR_ALIGNMENT
+    assert reduce_status(p[1] + 64, p, 1000) == tar.AR_ERR_OVERLAP             # partial overlap
+    assert reduce_status(out, p, 0) == tar.AR_ERR_NOT_INITIALIZED              # empty is valid
+
+
+def fused(**kw):
+    m, h = kw.pop("m", 16), kw.pop("h", 6144)
+    tb = m * h * 2
+    d = dict(partials=[BASE + i * 64 * MB for i in range(4)], residual_in=BASE + 4 * 64 * MB,
+             residual_out=BASE + 5 * 64 * MB, weight=BASE + 6 * 64 * MB, out=BASE + 7 * 64 * MB,
+             eps=1e-6, gemma=False, quant=False, q_out=None, scale_out=None, m=m, h=h,
+             dtype=tar.AR_DTYPE_BF16)
+    n_override = kw.pop("n", None)
+    d.update(kw)
+    assert tb < 64 * MB
+    a = tar.make_fused_args(**d)
+    if n_override is not None:
+        a.n = n_override
+    return tar.ar_fused_reduce_rmsnorm(None, a, None, raise_on_error=False)
+
+
+def test_fused_validation(lib):
+    NI = tar.AR_ERR_NOT_INITIALIZED
+    assert fused() == NI
+    assert fused(m=0) == NI                                             # empty batch is valid
+    assert fused(residual_in=None, residual_out=None) == NI
+    assert fused(residual_out=BASE + 4 * 64 * MB) == NI                 # residual_out == residual_in
+    assert fused(out=BASE) == NI                                        # out == partials[0] exactly
+    assert fused(quant=True, q_out=BASE + 8 * 64 * MB, scale_out=BASE + 9 * 64 * MB) == NI
+    assert fused(quant=True, out=None, q_out=BASE + 8 * 64 * MB, scale_out=BASE + 9 * 64 * MB) == NI
+    IA = tar.AR_ERR_INVALID_ARG
+    assert fused(h=0) == IA
+    assert fused(m=-1) == IA
+    assert fused(weight=None) == IA
+    assert fused(out=None) == IA                                        # no output without quant
+    assert fused(quant=True, q_out=None, scale_out=BASE + 9 * 64 * MB) == IA
+    assert fused(quant=True, q_out=BASE + 8 * 64 * MB, scale_out=None) == IA
+    assert fused(dtype=tar.AR_DTYPE_F32) == IA                          # fused is 16-bit only
+    assert fused(eps=float("nan")) == IA
+    assert fused(eps=-1.0) == IA
+    assert fused(eps=float("inf")) == IA
+    assert fused(partials=[]) == IA
+    assert fused(n=9) == IA
+    assert fused(partials=[BASE, 0, BASE + 64 * MB]) == IA
+    AL = tar.AR_ERR_ALIGNMENT
+    assert fused(out=BASE + 7 * 64 * MB + 1) == AL
+    assert fused(weight=BASE + 6 * 64 * MB + 1) == AL
+    assert fused(quant=True, q_out=BASE + 8 * 64 * MB, scale_out=BASE + 9 * 64 * MB + 2) == AL
+    OV = tar.AR_ERR_OVERLAP
+    assert fused(out=BASE + 32) == OV                                   # inside partials[0]
+    assert fused(residual_out=BASE + 7 * 64 * MB) == OV                 # residual_out == out
+    assert fused(out=BASE + 6 * 64 * MB) == OV                          # out on the weight
+    assert fused(quant=True, q_out=BASE, scale_out=BASE + 9 * 64 * MB) == OV  # codes over a partial
+    assert fused(quant=True, q_out=BASE + 8 * 64 * MB, scale_out=BASE + 8 * 64 * MB + 64) == OV
+
+
+def test_options_reject_out_of_range_values(lib):
+    # ar_set_option checks the context first; the value ranges are exercised on the GPU
+    assert lib.ar_set_option(None, 99, 0) == tar.AR_ERR_NOT_INITIALIZED
