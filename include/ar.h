@@ -34,7 +34,8 @@
  * launch; ar_last_error() gives the CUDA message.  Nothing throws across this ABI.
  *
  * Threads: one context may be used by one host thread at a time; distinct contexts
- * are independent.  A context holds no device memory.
+ * are independent.  A context owns one small device status word (see ar_device_status)
+ * and no other device memory.
  */
 #ifndef AR_H
 #define AR_H
@@ -90,7 +91,8 @@ ar_status ar_destroy(ar_ctx* ctx);
  * out:      device, numel elements of dtype; may equal partials[k] exactly (in place),
  *           must not overlap any partial otherwise.
  * partials: HOST array of n device pointers, each numel elements of dtype.
- * n:        1..AR_MAX_PARTIALS.   numel: >= 0 (0 launches nothing).
+ * n:        1..AR_MAX_PARTIALS.   numel: >= 0 (0 launches nothing and accepts any
+ *           pointer values, NULL included).
  * dtype:    AR_DTYPE_F32, AR_DTYPE_F16 or AR_DTYPE_BF16 (fp32: the fp32 sum is stored).
  * stream:   cudaStream_t (NULL = legacy default stream).
  * Pointers must be aligned to the element size; 16-byte-aligned pointers take the vector
@@ -120,7 +122,8 @@ typedef struct {
   int quant;                               /* AR_QUANT_NONE or AR_QUANT_FP8_E4M3_PER_TOKEN */
   void* q_out;                             /* device [m, h] E4M3 bytes, required when quant is on */
   float* scale_out;                        /* device [m] fp32 per-row scales, required when quant is on */
-  int64_t m;                               /* rows (tokens), >= 0 (0 launches nothing) */
+  int64_t m;                               /* rows (tokens), >= 0 (0 launches nothing; then
+                                              only weight must be non-NULL) */
   int64_t h;                               /* hidden size, >= 1 */
   ar_dtype dtype;                          /* AR_DTYPE_BF16 or AR_DTYPE_F16 */
 } ar_fused_args;
@@ -140,6 +143,15 @@ typedef struct {
  * is refused with AR_ERR_OVERLAP before anything is launched.
  */
 ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* args, void* stream);
+
+/*
+ * Read and clear the context's device status word.  The staged variant waits on its
+ * shared-memory copies with a bound (about a second); if a wait ever runs out, the kernel
+ * stops early, its outputs are incomplete, and it records code 1 here.  0 means no wait
+ * has run out since the last read.  Synchronises the device (a blocking copy): call it
+ * outside graph capture, e.g. after a batch of calls.  No counterpart on the pages.
+ */
+ar_status ar_device_status(ar_ctx* ctx, int* code);
 
 /* Static description of a status code. */
 const char* ar_status_string(ar_status s);

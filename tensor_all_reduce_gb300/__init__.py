@@ -97,8 +97,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ar_last_variant.restype = ctypes.c_char_p
     lib.ar_set_option.argtypes = [vp, c_int, i64]
     lib.ar_get_info.argtypes = [vp, c_int, ctypes.POINTER(i64)]
+    lib.ar_device_status.argtypes = [vp, ctypes.POINTER(c_int)]
     for f in ("ar_init", "ar_destroy", "ar_reduce_sum", "ar_fused_reduce_rmsnorm", "ar_set_option",
-              "ar_get_info"):
+              "ar_get_info", "ar_device_status"):
         getattr(lib, f).restype = c_int
     _lib = lib
     return lib
@@ -145,6 +146,15 @@ def ar_get_info(ctx: int, key: int) -> int:
     st = load_library().ar_get_info(ctx, int(key), ctypes.byref(v))
     if st != AR_OK:
         raise ArError(st, "ar_get_info")
+    return v.value
+
+
+def ar_device_status(ctx: int) -> int:
+    """Read and clear the context's device status word (0: no bounded wait ran out)."""
+    v = ctypes.c_int()
+    st = load_library().ar_device_status(ctx, ctypes.byref(v))
+    if st != AR_OK:
+        raise ArError(st, "ar_device_status")
     return v.value
 
 
@@ -245,6 +255,9 @@ class Context:
 
     def info(self, key: int) -> int:
         return ar_get_info(self.handle, key)
+
+    def device_status(self) -> int:
+        return ar_device_status(self.handle)
 
     def reduce_sum(self, partials, out=None, stream=None):
         """Sum contiguous same-shaped device tensors in rank order; returns `out`."""

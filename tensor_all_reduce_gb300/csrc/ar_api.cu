@@ -12,12 +12,15 @@
 #include "ar.h"
 #include "ar_common.cuh"
 #include "ar_launch.h"
+#include "ar_staged.cuh"
 
 struct ar_ctx {
   int device;
   int sm_count;
   int64_t l2_bytes;
   int max_cluster;       // largest cluster the fused kernel can be launched with
+  int max_dyn_smem;      // opt-in dynamic shared memory per block (bytes)
+  int* d_status;         // device status word of the staged kernel (0 = no timeout)
   // overrides (0 = automatic)
   int force_variant;
   int cluster_size;
@@ -62,12 +65,12 @@ ar_status fail_cuda(ar_ctx* ctx, cudaError_t e, const char* what) {
   return AR_ERR_CUDA;
 }
 
-ar_status launch(ar_ctx* ctx, const void* fn, unsigned grid, unsigned block, int csize, void* params,
-                 void* stream) {
+ar_status launch(ar_ctx* ctx, const void* fn, unsigned grid, unsigned block, int csize, void** args,
+                 size_t dyn_smem, void* stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid, 1, 1);
   cfg.blockDim = dim3(block, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = dyn_smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];
   if (csize > 1) {
@@ -78,7 +81,6 @@ ar_status launch(ar_ctx* ctx, const void* fn, unsigned grid, unsigned block, int
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  void* args[1] = {params};
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return fail_cuda(ctx, e, "kernel launch");
   return AR_OK;
@@ -98,6 +100,18 @@ int fused_kernel_list(const void** out, int cap) {
             const void* fn = dt ? fused_kernel_bf16(n, ppt, q != 0, v != 0) : fused_kernel_f16(n, ppt, q != 0, v != 0);
             if (fn && k < cap) out[k++] = fn;
           }
+  return k;
+}
+
+int staged_kernel_list(const void** out, int cap) {
+  int k = 0;
+  for (int dt = 0; dt < 2; ++dt)
+    for (int n = 1; n <= AR_MAX_PARTIALS; ++n)
+      for (int ppt = 2; ppt <= 4; ppt *= 2)
+        for (int q = 0; q < 2; ++q) {
+          const void* fn = dt ? staged_kernel_bf16(n, ppt, q != 0) : staged_kernel_f16(n, ppt, q != 0);
+          if (fn && k < cap) out[k++] = fn;
+        }
   return k;
 }
 }  // namespace ar
@@ -169,6 +183,30 @@ ar_status ar_init(ar_ctx** out, int device, unsigned flags) {
               return AR_ERR_CUDA;
             }
           }
+  // Staged kernels: allow the opt-in shared memory size; one status word for their
+  // bounded waits (the only device memory a context owns).
+  {
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) {
+      free(ctx);
+      return AR_ERR_CUDA;
+    }
+    ctx->max_dyn_smem = optin - 1024;  // room for the kernels' static shared memory
+    nf = ar::staged_kernel_list(fns, 512);
+    for (int i = 0; i < nf; ++i) {
+      e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, ctx->max_dyn_smem);
+      if (e != cudaSuccess) {
+        free(ctx);
+        return AR_ERR_CUDA;
+      }
+    }
+    if (cudaMalloc(&ctx->d_status, 256) != cudaSuccess || cudaMemset(ctx->d_status, 0, 256) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+      if (ctx->d_status) cudaFree(ctx->d_status);
+      free(ctx);
+      return AR_ERR_CUDA;
+    }
+  }
   // Largest cluster the fused kernel supports with a small block on this device.
   {
     cudaLaunchConfig_t cfg = {};
@@ -193,7 +231,28 @@ ar_status ar_init(ar_ctx** out, int device, unsigned flags) {
 }
 
 ar_status ar_destroy(ar_ctx* ctx) {
-  free(ctx);
+  if (ctx) {
+    if (ctx->d_status) {
+      DeviceGuard g(ctx->device);
+      cudaFree(ctx->d_status);
+    }
+    free(ctx);
+  }
+  return AR_OK;
+}
+
+ar_status ar_device_status(ar_ctx* ctx, int* code) {
+  if (!code) return AR_ERR_INVALID_ARG;
+  if (!ctx) return AR_ERR_NOT_INITIALIZED;
+  DeviceGuard g(ctx->device);
+  int v = 0;
+  cudaError_t e = cudaMemcpy(&v, ctx->d_status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return fail_cuda(ctx, e, "status read");
+  if (v != 0) {
+    e = cudaMemset(ctx->d_status, 0, sizeof(int));
+    if (e != cudaSuccess) return fail_cuda(ctx, e, "status reset");
+  }
+  *code = v;
   return AR_OK;
 }
 
@@ -244,8 +303,13 @@ ar_status ar_get_info(const ar_ctx* ctx, ar_info key, int64_t* value) {
 
 ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int n, int64_t numel,
                         ar_dtype dtype, void* stream) {
-  if (!out || !partials || n < 1 || n > AR_MAX_PARTIALS || numel < 0 || !dtype_ok(dtype))
-    return AR_ERR_INVALID_ARG;
+  if (!partials || n < 1 || n > AR_MAX_PARTIALS || numel < 0 || !dtype_ok(dtype)) return AR_ERR_INVALID_ARG;
+  if (numel == 0) {  // nothing is touched: any pointer (NULL included) is acceptable
+    if (!ctx) return AR_ERR_NOT_INITIALIZED;
+    ctx->last_variant = "none";
+    return AR_OK;
+  }
+  if (!out) return AR_ERR_INVALID_ARG;
   const int es = elem_size(dtype);
   if (numel > INT64_MAX / 16) return AR_ERR_INVALID_ARG;
   const int64_t bytes = numel * es;
@@ -256,10 +320,6 @@ ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int
     if (partials[r] != out && overlaps(out, bytes, partials[r], bytes)) return AR_ERR_OVERLAP;
   }
   if (!ctx) return AR_ERR_NOT_INITIALIZED;
-  if (numel == 0) {
-    ctx->last_variant = "none";
-    return AR_OK;
-  }
 
   ar::ReduceParams p;
   memset(&p, 0, sizeof(p));
@@ -296,7 +356,8 @@ ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int
     name = "reduce_scalar";
   }
   if (!fn) return AR_ERR_UNSUPPORTED;
-  ar_status st = launch(ctx, fn, grid, kReduceBlock, 1, &p, stream);
+  void* args[1] = {&p};
+  ar_status st = launch(ctx, fn, grid, kReduceBlock, 1, args, 0, stream);
   if (st == AR_OK) ctx->last_variant = name;
   return st;
 }
@@ -311,10 +372,15 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   if (a->dtype != AR_DTYPE_BF16 && a->dtype != AR_DTYPE_F16) return AR_ERR_INVALID_ARG;
   if (a->quant != AR_QUANT_NONE && a->quant != AR_QUANT_FP8_E4M3_PER_TOKEN) return AR_ERR_INVALID_ARG;
   const bool quant = a->quant == AR_QUANT_FP8_E4M3_PER_TOKEN;
-  if (quant && (!a->q_out || !a->scale_out)) return AR_ERR_INVALID_ARG;
-  if (!quant && !a->out) return AR_ERR_INVALID_ARG;
   if (!(a->eps >= 0.0f) || isinf(a->eps)) return AR_ERR_INVALID_ARG;  // also rejects NaN
   if (a->h > (int64_t)1 << 30 || a->m > ((int64_t)1 << 40) / a->h) return AR_ERR_INVALID_ARG;
+  if (a->m == 0) {  // no rows: only the weight is a real buffer; nothing is touched
+    if (!ctx) return AR_ERR_NOT_INITIALIZED;
+    ctx->last_variant = "none";
+    return AR_OK;
+  }
+  if (quant && (!a->q_out || !a->scale_out)) return AR_ERR_INVALID_ARG;
+  if (!quant && !a->out) return AR_ERR_INVALID_ARG;
   for (int r = 0; r < a->n; ++r)
     if (!a->partials[r]) return AR_ERR_INVALID_ARG;
 
@@ -353,10 +419,6 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
       if (overlaps(outs[o].p, outs[o].n, outs[o2].p, outs[o2].n)) return AR_ERR_OVERLAP;
   }
   if (!ctx) return AR_ERR_NOT_INITIALIZED;
-  if (a->m == 0) {
-    ctx->last_variant = "none";
-    return AR_OK;
-  }
 
   // ---- variant selection ----
   bool vec = (a->h % 8) == 0;
@@ -367,6 +429,49 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
 
   const int row_packs = (int)((a->h + 7) / 8);
   const int max_cl = ctx->max_cluster;
+
+  // ---- staged (bulk-copy pipelined) variant: only when forced for now ----
+  if (ctx->force_variant == 3) {
+    const int rows_per_stage = a->n + (a->residual_in ? 1 : 0);
+    const int64_t stage_bytes = (int64_t)rows_per_stage * a->h * es;
+    int S = ctx->stages ? ctx->stages : (int)(ctx->max_dyn_smem / stage_bytes);
+    if (S > 4) S = 4;
+    if (!vec || row_packs > 1024 || S < 2 || S * stage_bytes > ctx->max_dyn_smem) return AR_ERR_UNSUPPORTED;
+    const int sppt = ctx->ppt == 4 ? 4 : 2;
+    int sblock = ((row_packs + sppt - 1) / sppt + 31) / 32 * 32;
+    if (sblock < 32) sblock = 32;
+    ar::FusedParams p;
+    memset(&p, 0, sizeof(p));
+    for (int r = 0; r < a->n; ++r) p.x[r] = a->partials[r];
+    p.res_in = a->residual_in;
+    p.res_out = a->residual_out;
+    p.w = a->weight;
+    p.out = a->out;
+    p.q = static_cast<uint8_t*>(a->q_out);
+    p.scale = a->scale_out;
+    p.m = a->m;
+    p.h = (int)a->h;
+    p.row_packs = row_packs;
+    p.chunk_packs = row_packs;
+    p.csize = 1;
+    p.eps = a->eps;
+    p.inv_h = (float)(1.0 / (double)a->h);
+    p.gemma = a->gemma != 0;
+    ar::StagedParams sp;
+    sp.stages = S;
+    sp.row_bytes = (int)(a->h * es);
+    sp.err = ctx->d_status;
+    sp.wait_cycles = 2000000000LL;  // about one second at the SM clock
+    const void* fn = a->dtype == AR_DTYPE_BF16 ? ar::staged_kernel_bf16(a->n, sppt, quant)
+                                               : ar::staged_kernel_f16(a->n, sppt, quant);
+    if (!fn) return AR_ERR_UNSUPPORTED;
+    const int64_t grid = a->m < ctx->sm_count ? a->m : ctx->sm_count;
+    DeviceGuard g(ctx->device);
+    void* args[2] = {&p, &sp};
+    ar_status st = launch(ctx, fn, (unsigned)grid, (unsigned)sblock, 1, args, (size_t)(S * stage_bytes), stream);
+    if (st == AR_OK) ctx->last_variant = "fused_staged";
+    return st;
+  }
   int csize;
   if (ctx->cluster_size) {
     csize = ctx->cluster_size;
@@ -416,7 +521,8 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
                                              : ar::fused_kernel_f16(a->n, ppt, quant, vec);
   if (!fn) return AR_ERR_UNSUPPORTED;
   DeviceGuard g(ctx->device);
-  ar_status st = launch(ctx, fn, (unsigned)grid, (unsigned)block, csize, &p, stream);
+  void* args[1] = {&p};
+  ar_status st = launch(ctx, fn, (unsigned)grid, (unsigned)block, csize, args, 0, stream);
   if (st == AR_OK) {
     if (vec)
       ctx->last_variant = csize > 1 ? "fused_cluster_vec" : "fused_row_vec";

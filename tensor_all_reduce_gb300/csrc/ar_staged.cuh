@@ -1,0 +1,245 @@
+// Staged large-M variant of the fused kernel: persistent CTAs, bulk asynchronous copies of
+// whole rows into shared memory, S-deep pipeline.
+//
+// Same arithmetic as fused_kernel (ar_fused.cuh); only the data movement differs.  One
+// CTA per SM loops over rows r = blockIdx.x + i * gridDim.x.  For each row one thread
+// issues a bulk global->shared copy (cp.async.bulk, the non-tensor form of TMA) of the
+// N partial rows and the residual row into stage i % S and arms the stage's mbarrier with
+// the byte count; while the CTA works on row i, rows i+1 .. i+S-1 are in flight.  A stage
+// is refilled as soon as the row's square-sum has been reduced (by then every thread has
+// read its packs), so loads for later rows overlap the normalisation and the stores.
+// The weight packs a thread needs never change across rows and live in registers.
+//
+// Full tiles only (page "[HIP] [Perf] Specialize partial tiles in two-stage custom
+// all-reduce", Proposed modifications: every thread executes the same number of
+// barriers): the loop trip count is per CTA, identical for all its threads, and every
+// barrier sits outside any per-thread predicate.
+//
+// Waits are bounded: a wait on a stage's mbarrier gives up after `wait_cycles` SM clock
+// cycles, the CTA agrees on the failure with __syncthreads_or, records code 1 in
+// `err`, waits (bounded again) for its own copies still in flight, and returns.
+#pragma once
+
+#include "ar_common.cuh"
+
+namespace ar {
+
+struct StagedParams {
+  int stages;             // S, 2..4
+  int row_bytes;          // h * 2
+  int* err;               // device status word (0 = fine), written only on a timeout
+  long long wait_cycles;  // bound of one mbarrier wait
+};
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Poll until the phase with `parity` completes or the cycle budget runs out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, long long budget) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > budget) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst_smem)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+
+template <int DT, int N, int PPT, bool QUANT>
+__global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedParams p, const StagedParams sp) {
+  extern __shared__ __align__(128) uint8_t stage_mem[];
+  __shared__ __align__(8) uint64_t full_bar[4];
+  __shared__ float red_ss[2][32];
+  __shared__ float red_amax[2][32];
+
+  const int S = sp.stages;
+  const bool has_res = p.res_in != nullptr;
+  const int rows_per_stage = N + (has_res ? 1 : 0);
+  const uint32_t row_bytes = (uint32_t)sp.row_bytes;
+  const uint32_t stage_bytes = row_bytes * (uint32_t)rows_per_stage;
+  const int64_t first = blockIdx.x, stride = gridDim.x;
+  const int64_t my_rows = first < p.m ? (p.m - first + stride - 1) / stride : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full_bar[s], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  auto issue = [&](int s, int64_t row) {
+    uint8_t* dst = stage_mem + (size_t)s * stage_bytes;
+    mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
+    const size_t off = (size_t)row * row_bytes;
+#pragma unroll
+    for (int r = 0; r < N; ++r) bulk_g2s(dst + (size_t)r * row_bytes, (const uint8_t*)p.x[r] + off, row_bytes, &full_bar[s]);
+    if (has_res) bulk_g2s(dst + (size_t)N * row_bytes, (const uint8_t*)p.res_in + off, row_bytes, &full_bar[s]);
+  };
+
+  if (threadIdx.x == 0) {
+    const int64_t pre = my_rows < S ? my_rows : S;
+    for (int64_t i = 0; i < pre; ++i) issue((int)i, first + i * stride);
+  }
+
+  // this thread's packs (fixed across rows) and their weights
+  bool valid[PPT];
+  uint4 wpk[PPT];
+#pragma unroll
+  for (int k = 0; k < PPT; ++k) {
+    const int pk = (int)threadIdx.x + k * (int)blockDim.x;
+    valid[k] = pk < p.row_packs;
+    const int pkc = valid[k] ? pk : 0;
+    wpk[k] = ld_keep(static_cast<const uint16_t*>(p.w) + (int64_t)pkc * 8);
+  }
+
+  for (int64_t i = 0; i < my_rows; ++i) {
+    const int s = (int)(i % S);
+    const uint32_t parity = (uint32_t)((i / S) & 1);
+    const int64_t row = first + i * stride;
+    const bool ok = mbar_wait_bounded(&full_bar[s], parity, sp.wait_cycles);
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) atomicExch(sp.err, 1);
+      // let this CTA's own copies still in flight land before shared memory is released
+      for (int64_t j = i; j < my_rows && j < i + S; ++j)
+        (void)mbar_wait_bounded(&full_bar[j % S], (uint32_t)((j / S) & 1), sp.wait_cycles);
+      return;
+    }
+    const uint8_t* st = stage_mem + (size_t)s * stage_bytes;
+    const int64_t row_e = row * (int64_t)p.h;
+
+    uint4 z[PPT];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+      const int pk = (int)threadIdx.x + k * (int)blockDim.x;
+      const int pkc = valid[k] ? pk : 0;
+      float acc[8];
+      unpack8<DT>(lds_v4(st + (size_t)pkc * 16), acc);
+#pragma unroll
+      for (int r = 1; r < N; ++r) {
+        float t[8];
+        unpack8<DT>(lds_v4(st + (size_t)r * row_bytes + (size_t)pkc * 16), t);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = acc[e] + t[e];
+      }
+      uint4 sv = pack8<DT>(acc);
+      if (has_res) {
+        float sf[8], rf[8];
+        unpack8<DT>(sv, sf);
+        unpack8<DT>(lds_v4(st + (size_t)N * row_bytes + (size_t)pkc * 16), rf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sf[e] = sf[e] + rf[e];
+        sv = pack8<DT>(sf);
+      }
+      z[k] = sv;
+      if (valid[k]) {
+        float zf[8];
+        unpack8<DT>(sv, zf);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(zf[e], zf[e], ss);
+      }
+    }
+    const float tot = block_allreduce<false>(ss, red_ss[i & 1]);
+    // every thread has read stage s: refill it with the row S iterations ahead
+    if (threadIdx.x == 0 && i + S < my_rows) {
+      fence_proxy_async_smem();
+      issue(s, first + (i + S) * stride);
+    }
+    if (p.res_out != nullptr) {
+#pragma unroll
+      for (int k = 0; k < PPT; ++k)
+        if (valid[k]) st_v4(static_cast<uint16_t*>(p.res_out) + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8, z[k]);
+    }
+    const float inv = rsqrtf(tot * p.inv_h + p.eps);
+    uint4 y[PPT];
+    float amax = 0.0f;
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+      float zf[8], wf[8], yf[8];
+      unpack8<DT>(z[k], zf);
+      unpack8<DT>(wpk[k], wf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float wv = p.gemma ? 1.0f + wf[e] : wf[e];
+        yf[e] = (zf[e] * inv) * wv;
+      }
+      y[k] = pack8<DT>(yf);
+      if (QUANT && valid[k]) {
+        float yr[8];
+        unpack8<DT>(y[k], yr);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(yr[e]));
+      }
+    }
+    if (p.out != nullptr) {
+#pragma unroll
+      for (int k = 0; k < PPT; ++k)
+        if (valid[k]) st_v4(static_cast<uint16_t*>(p.out) + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8, y[k]);
+    }
+    if constexpr (QUANT) {
+      const float am = block_allreduce<true>(amax, red_amax[i & 1]);
+      const float scale = __fdiv_rn(am, 448.0f);
+      if (threadIdx.x == 0) st_f32(p.scale + row, scale);
+#pragma unroll
+      for (int k = 0; k < PPT; ++k) {
+        if (!valid[k]) continue;
+        float yr[8];
+        unpack8<DT>(y[k], yr);
+        uint32_t c[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = am == 0.0f ? 0.0f : __fdiv_rn(yr[2 * e], scale);
+          const float b = am == 0.0f ? 0.0f : __fdiv_rn(yr[2 * e + 1], scale);
+          c[e] = e4m3x2(a, b);
+        }
+        st_v2(p.q + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8,
+              make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16)));
+      }
+    }
+  }
+}
+
+}  // namespace ar

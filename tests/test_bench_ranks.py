@@ -1,0 +1,76 @@
+"""The benchmark's multi-rank logic on CPU: two gloo ranks, each an independent replica.
+
+The path has no exchange between GPUs (rows are independent and every rank holds its own
+partials), so ranks only meet at the timing barriers and in the max over ranks.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    dist = bench.init_dist(world, "gloo")
+    local_ms = 10.0 + 5.0 * rank           # rank 1 is the slow replica
+    bench.barrier(world)
+    m = bench.max_over_ranks(local_ms, world)
+    q.put((rank, m, bench.job_us_per_call(m, 100, world)))
+    dist.destroy_process_group()
+
+
+def test_max_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    # both ranks see the slowest replica's time; the job time per call spans both ranks' calls
+    assert [g[1] for g in got] == [15.0, 15.0]
+    assert got[0][2] == pytest.approx(15.0 * 1000 / 200)
+
+
+def test_rotation_sets_cover_l2():
+    sys.path.insert(0, ROOT)
+    import bench
+    l2 = 126 * 2**20
+    assert bench.rotation_sets(258 * 10**6, l2) == 2
+    assert bench.rotation_sets(10**9, l2) == 1
+    assert bench.rotation_sets(98_304, l2, cap=4096) == 4032
+    assert bench.rotation_sets(10, l2, cap=64) == 64
+
+
+def test_reference_arm_under_two_ranks_only_rank0_prints():
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr=127.0.0.1", f"--master-port={port}", os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "3", "--warmup", "3",
+           "--workload", "n4_m16_h6144_bf16_plain"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [json.loads(line) for line in r.stdout.splitlines() if line.startswith("{")]
+    assert len(lines) == 1
+    line = lines[0]
+    assert line["impl"] == "reference" and line["unit"] == "us/call" and line["higher_is_better"] is False
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0

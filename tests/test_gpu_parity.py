@@ -142,12 +142,15 @@ def test_fused_tail_hidden_sizes(ctx, dev, orc, dtype, h):
 VARIANTS = ([("row", {tar.AR_OPT_FORCE_VARIANT: tar.VARIANT_ROW, tar.AR_OPT_PACKS_PER_THREAD: p}) for p in (1, 2, 4)]
             + [(f"cluster{c}", {tar.AR_OPT_CLUSTER_SIZE: c}) for c in (2, 4, 8, 16)]
             + [("cluster8_ppt2", {tar.AR_OPT_CLUSTER_SIZE: 8, tar.AR_OPT_PACKS_PER_THREAD: 2})]
+            + [("staged", {tar.AR_OPT_FORCE_VARIANT: tar.VARIANT_STAGED}),
+               ("staged_s2_ppt4", {tar.AR_OPT_FORCE_VARIANT: tar.VARIANT_STAGED, tar.AR_OPT_STAGES: 2,
+                                   tar.AR_OPT_PACKS_PER_THREAD: 4})]
             + [("scalar", {tar.AR_OPT_FORCE_VARIANT: tar.VARIANT_SCALAR}),
                ("scalar_cluster4", {tar.AR_OPT_FORCE_VARIANT: tar.VARIANT_SCALAR, tar.AR_OPT_CLUSTER_SIZE: 4})])
 
 
 @pytest.mark.parametrize("name,opts", VARIANTS, ids=[v[0] for v in VARIANTS])
-@pytest.mark.parametrize("m,h", [(33, 6144), (3, 7168), (2, 2880)])
+@pytest.mark.parametrize("m,h", [(33, 6144), (3, 7168), (2, 2880), (700, 4096)])
 def test_fused_every_variant(ctx, dev, orc, name, opts, m, h):
     for k, v in opts.items():
         ctx.set_option(k, v)
@@ -158,6 +161,9 @@ def test_fused_every_variant(ctx, dev, orc, name, opts, m, h):
         check_fused(orc, got, ref, "bf16", quant)
         if "cluster" in name:
             assert "cluster" in got["variant"], got["variant"]
+        elif name.startswith("staged"):
+            assert got["variant"] == "fused_staged"
+            assert ctx.device_status() == 0
         elif name == "scalar":
             assert "scalar" in got["variant"]
         else:
@@ -217,6 +223,24 @@ def test_fused_aliases(ctx, dev, orc):
     torch.cuda.synchronize()
     assert_bits_equal(bits_of(res), ref["res_out"], "residual_out in place")
     assert_y_within_ulp(bits_of(parts[0]), ref["y"], "bf16")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("n", [1, 4, 8])
+def test_fused_staged_large(ctx, dev, orc, n, dtype):
+    """The staged variant on large batches: many rows per CTA, every pipeline stage reused."""
+    ctx.set_option(tar.AR_OPT_FORCE_VARIANT, tar.VARIANT_STAGED)
+    for quant in (False, True):
+        inp = synth.fused_inputs(n, 1500, 6144, dtype, seed=n * 3 + quant, gemma=quant)
+        got = run_fused(ctx, dev, inp, dtype, gemma=quant, quant=quant)
+        assert got["variant"] == "fused_staged"
+        check_fused(orc, got, oracle_fused(orc, inp, dtype, gemma=quant, quant=quant), dtype, quant)
+    inp = synth.fused_inputs(n, 777, 4096, dtype, seed=n, residual=False)
+    got = run_fused(ctx, dev, inp, dtype)
+    ref = orc.fused([synth.bits(p) for p in inp["partials"]], None, synth.bits(inp["weight"]), 1e-6, False,
+                    False, dtype)
+    check_fused(orc, got, ref, dtype, False)
+    assert ctx.device_status() == 0
 
 
 def test_fused_empty_batch(ctx, dev):
