@@ -430,13 +430,19 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   const int row_packs = (int)((a->h + 7) / 8);
   const int max_cl = ctx->max_cluster;
 
-  // ---- staged (bulk-copy pipelined) variant: only when forced for now ----
-  if (ctx->force_variant == 3) {
-    const int rows_per_stage = a->n + (a->residual_in ? 1 : 0);
-    const int64_t stage_bytes = (int64_t)rows_per_stage * a->h * es;
-    int S = ctx->stages ? ctx->stages : (int)(ctx->max_dyn_smem / stage_bytes);
-    if (S > 4) S = 4;
-    if (!vec || row_packs > 1024 || S < 2 || S * stage_bytes > ctx->max_dyn_smem) return AR_ERR_UNSUPPORTED;
+  // ---- staged (bulk-copy pipelined, persistent) variant for large batches ----
+  const int rows_per_stage = a->n + (a->residual_in ? 1 : 0);
+  const int64_t stage_bytes = (int64_t)rows_per_stage * a->h * es;
+  // enough stages for ~96 KB in flight per SM, within the shared memory
+  int S = ctx->stages ? ctx->stages : (int)((96 * 1024 + stage_bytes - 1) / stage_bytes);
+  if (S < 2) S = 2;
+  if (S > 4) S = 4;
+  while (!ctx->stages && S > 2 && S * stage_bytes > ctx->max_dyn_smem) --S;
+  const bool staged_ok = vec && row_packs <= 1024 && S * stage_bytes <= ctx->max_dyn_smem;
+  const bool staged_auto = ctx->force_variant == 0 && ctx->cluster_size == 0 && ctx->ppt == 0 &&
+                           a->m >= 4LL * ctx->sm_count;
+  if (ctx->force_variant == 3 || (staged_auto && staged_ok)) {
+    if (!staged_ok) return AR_ERR_UNSUPPORTED;
     const int sppt = ctx->ppt == 4 ? 4 : 2;
     int sblock = ((row_packs + sppt - 1) / sppt + 31) / 32 * 32;
     if (sblock < 32) sblock = 32;

@@ -173,6 +173,20 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
+// Correctly rounded y / d from r = RN(1/d) with one correction step (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): q0 = RN(y r) is within an ulp of y / d, the remainder y - q0 d is
+// exact through the fused multiply-add, and RN(q0 + rem r) is RN(y / d) when r is the
+// correctly rounded reciprocal and the quotient is in the normal range.  A binary quotient
+// is never exactly half-way between two floats, so there are no ties to break.  Used for
+// the per-element FP8 quotient, where it replaces an IEEE division per element by three
+// multiply-adds; quotients below the normal range round to FP8 zero either way.
+__device__ __forceinline__ float div_rn_by(float y, float d, float r) {
+  const float q0 = y * r;
+  const float rem = fmaf(-q0, d, y);
+  return fmaf(rem, r, q0);
+}
+
 // ---------------------------------------------------------------------------
 // reductions
 // ---------------------------------------------------------------------------

@@ -176,6 +176,8 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
     }
     const float scale = __fdiv_rn(am, 448.0f);
     if (crank == 0 && threadIdx.x == 0) st_f32(p.scale + row, scale);
+    // an all-zero row has scale 0 and all codes 0 (no division)
+    const float rcp = am == 0.0f ? 0.0f : __frcp_rn(scale);
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
       if (!valid[k]) continue;
@@ -185,8 +187,8 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
       uint32_t c[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const float a = am == 0.0f ? 0.0f : __fdiv_rn(yr[2 * i], scale);
-        const float b = am == 0.0f ? 0.0f : __fdiv_rn(yr[2 * i + 1], scale);
+        const float a = am == 0.0f ? 0.0f : div_rn_by(yr[2 * i], scale, rcp);
+        const float b = am == 0.0f ? 0.0f : div_rn_by(yr[2 * i + 1], scale, rcp);
         c[i] = e4m3x2(a, b);
       }
       const int64_t e0 = row_e + (int64_t)pk * 8;

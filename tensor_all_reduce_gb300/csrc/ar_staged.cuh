@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
       const float am = block_allreduce<true>(amax, red_amax[i & 1]);
       const float scale = __fdiv_rn(am, 448.0f);
       if (threadIdx.x == 0) st_f32(p.scale + row, scale);
+      const float rcp = am == 0.0f ? 0.0f : __frcp_rn(scale);
 #pragma unroll
       for (int k = 0; k < PPT; ++k) {
         if (!valid[k]) continue;
@@ -231,8 +232,8 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
         uint32_t c[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float a = am == 0.0f ? 0.0f : __fdiv_rn(yr[2 * e], scale);
-          const float b = am == 0.0f ? 0.0f : __fdiv_rn(yr[2 * e + 1], scale);
+          const float a = am == 0.0f ? 0.0f : div_rn_by(yr[2 * e], scale, rcp);
+          const float b = am == 0.0f ? 0.0f : div_rn_by(yr[2 * e + 1], scale, rcp);
           c[e] = e4m3x2(a, b);
         }
         st_v2(p.q + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8,

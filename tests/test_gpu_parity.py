@@ -199,6 +199,24 @@ def test_fused_options(ctx, dev, orc):
         check_fused(orc, got, oracle_fused(orc, inp, "fp16", eps=eps), "fp16", False)
 
 
+@pytest.mark.parametrize("variant", [tar.VARIANT_ROW, tar.VARIANT_STAGED, tar.VARIANT_CLUSTER, tar.VARIANT_SCALAR])
+def test_fp8_codes_exact_given_y(ctx, dev, orc, variant):
+    """The kernels quantise with a correctly rounded quotient, so given the kernel's own y
+    the codes and scales equal the oracle's exactly (the contract allows one code)."""
+    ctx.set_option(tar.AR_OPT_FORCE_VARIANT, variant)
+    inp = synth.fused_inputs(4, 700, 4096, "bf16", seed=21, gemma=True)
+    # rows spanning many magnitudes, so scales cover many binades
+    g = torch.Generator().manual_seed(5)
+    mags = (2.0 ** torch.randint(-12, 12, (700, 1), generator=g)).to(torch.float32)
+    inp["weight"] = (inp["weight"].float() * 3).to(torch.bfloat16)
+    inp["partials"] = [(p.float() * mags).to(torch.bfloat16) for p in inp["partials"]]
+    inp["residual"] = (inp["residual"].float() * mags).to(torch.bfloat16)
+    got = run_fused(ctx, dev, inp, "bf16", gemma=True, quant=True)
+    q_ref, s_ref = orc.per_token_quant(got["y"], "bf16")
+    assert np.array_equal(got["scale"].view(np.uint32), s_ref.view(np.uint32))
+    assert np.array_equal(got["q"], q_ref)
+
+
 def test_fused_zero_row_and_saturation(ctx, dev, orc):
     inp = synth.fused_inputs(4, 6, 2048, "bf16", seed=6, gemma=True)
     for p in inp["partials"]:
