@@ -171,7 +171,7 @@ typedef enum {
   AR_OPT_CLUSTER_SIZE = 1,   /* 0 auto, else 1, 2, 4, 8 or 16 CTAs per row */
   AR_OPT_PACKS_PER_THREAD = 2, /* 0 auto, else 1, 2 or 4 16-byte packs per thread */
   AR_OPT_REDUCE_UNROLL = 3,  /* 0 auto, else 1, 2 or 4 packs per thread per tile */
-  AR_OPT_STAGES = 4          /* 0 auto, else 2..4 shared-memory stages (staged variant) */
+  AR_OPT_STAGES = 4          /* 0 auto, else 1..4 shared-memory stages per CTA (staged variant) */
 } ar_option;
 ar_status ar_set_option(ar_ctx* ctx, ar_option opt, int64_t value);
 

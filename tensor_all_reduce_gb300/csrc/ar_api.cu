@@ -107,7 +107,7 @@ int staged_kernel_list(const void** out, int cap) {
   int k = 0;
   for (int dt = 0; dt < 2; ++dt)
     for (int n = 1; n <= AR_MAX_PARTIALS; ++n)
-      for (int ppt = 2; ppt <= 4; ppt *= 2)
+      for (int ppt = 1; ppt <= 4; ppt *= 2)
         for (int q = 0; q < 2; ++q) {
           const void* fn = dt ? staged_kernel_bf16(n, ppt, q != 0) : staged_kernel_f16(n, ppt, q != 0);
           if (fn && k < cap) out[k++] = fn;
@@ -276,7 +276,7 @@ ar_status ar_set_option(ar_ctx* ctx, ar_option opt, int64_t v) {
       ctx->reduce_unroll = (int)v;
       return AR_OK;
     case AR_OPT_STAGES:
-      if (!(v == 0 || (v >= 2 && v <= 4))) return AR_ERR_INVALID_ARG;
+      if (!(v == 0 || (v >= 1 && v <= 4))) return AR_ERR_INVALID_ARG;
       ctx->stages = (int)v;
       return AR_OK;
   }
@@ -433,17 +433,20 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   // ---- staged (bulk-copy pipelined, persistent) variant for large batches ----
   const int rows_per_stage = a->n + (a->residual_in ? 1 : 0);
   const int64_t stage_bytes = (int64_t)rows_per_stage * a->h * es;
-  // enough stages for ~96 KB in flight per SM, within the shared memory
-  int S = ctx->stages ? ctx->stages : (int)((96 * 1024 + stage_bytes - 1) / stage_bytes);
-  if (S < 2) S = 2;
-  if (S > 4) S = 4;
-  while (!ctx->stages && S > 2 && S * stage_bytes > ctx->max_dyn_smem) --S;
+  // Stages per CTA: with the FP8 epilogue one stage per CTA and several CTAs per SM hide
+  // the longer per-row work best; without it two stages in one CTA per SM stream best
+  // (measured on GB300 at N = 4 and 8, h = 6144 and 7168).
+  int S = ctx->stages ? ctx->stages : (quant ? 1 : 2);
+  if (!ctx->stages && S * stage_bytes > ctx->max_dyn_smem) S = 1;
   const bool staged_ok = vec && row_packs <= 1024 && S * stage_bytes <= ctx->max_dyn_smem;
+  // Automatic choice: fewer rows than SMs -> one staged CTA per row (bulk row loads have
+  // the lowest latency); 1..4 rows per SM -> the row kernel; more -> the persistent staged
+  // kernel.
   const bool staged_auto = ctx->force_variant == 0 && ctx->cluster_size == 0 && ctx->ppt == 0 &&
-                           a->m >= 4LL * ctx->sm_count;
+                           (a->m < ctx->sm_count || a->m >= 4LL * ctx->sm_count);
   if (ctx->force_variant == 3 || (staged_auto && staged_ok)) {
     if (!staged_ok) return AR_ERR_UNSUPPORTED;
-    const int sppt = ctx->ppt == 4 ? 4 : 2;
+    const int sppt = ctx->ppt ? ctx->ppt : 2;
     int sblock = ((row_packs + sppt - 1) / sppt + 31) / 32 * 32;
     if (sblock < 32) sblock = 32;
     ar::FusedParams p;
@@ -471,8 +474,15 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
     const void* fn = a->dtype == AR_DTYPE_BF16 ? ar::staged_kernel_bf16(a->n, sppt, quant)
                                                : ar::staged_kernel_f16(a->n, sppt, quant);
     if (!fn) return AR_ERR_UNSUPPORTED;
-    const int64_t grid = a->m < ctx->sm_count ? a->m : ctx->sm_count;
     DeviceGuard g(ctx->device);
+    // persistent grid: as many CTAs as fit on the SMs at once (shared memory bound)
+    int per_sm = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, sblock, (size_t)(S * stage_bytes)) !=
+            cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    const int64_t slots = (int64_t)ctx->sm_count * per_sm;
+    const int64_t grid = a->m < slots ? a->m : slots;
     void* args[2] = {&p, &sp};
     ar_status st = launch(ctx, fn, (unsigned)grid, (unsigned)sblock, 1, args, (size_t)(S * stage_bytes), stream);
     if (st == AR_OK) ctx->last_variant = "fused_staged";

@@ -180,11 +180,13 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // correctly rounded reciprocal and the quotient is in the normal range.  A binary quotient
 // is never exactly half-way between two floats, so there are no ties to break.  Used for
 // the per-element FP8 quotient, where it replaces an IEEE division per element by three
-// multiply-adds; quotients below the normal range round to FP8 zero either way.
+// multiply-adds; quotients below the normal range round to FP8 zero either way.  The
+// correction of a zero quotient would return +0 for y = -0 ((+0) + (-0) = +0), so the
+// sign is taken from y, as IEEE division keeps it.
 __device__ __forceinline__ float div_rn_by(float y, float d, float r) {
   const float q0 = y * r;
   const float rem = fmaf(-q0, d, y);
-  return fmaf(rem, r, q0);
+  return copysignf(fmaf(rem, r, q0), y);
 }
 
 // ---------------------------------------------------------------------------

@@ -14,7 +14,7 @@ const void* reduce_kernel(int dtype, int n, int unroll, bool vec, bool has_tail)
 const void* fused_kernel_f16(int n, int ppt, bool quant, bool vec);
 const void* fused_kernel_bf16(int n, int ppt, bool quant, bool vec);
 
-// Staged (bulk-copy pipelined, persistent) fused kernel: n in 1..8, ppt 2 or 4.
+// Staged (bulk-copy pipelined, persistent) fused kernel: n in 1..8, ppt 1, 2 or 4.
 const void* staged_kernel_f16(int n, int ppt, bool quant);
 const void* staged_kernel_bf16(int n, int ppt, bool quant);
 

@@ -1,11 +1,14 @@
 // Staged large-M variant of the fused kernel: persistent CTAs, bulk asynchronous copies of
 // whole rows into shared memory, S-deep pipeline.
 //
-// Same arithmetic as fused_kernel (ar_fused.cuh); only the data movement differs.  One
-// CTA per SM loops over rows r = blockIdx.x + i * gridDim.x.  For each row one thread
+// Same arithmetic as fused_kernel (ar_fused.cuh); only the data movement differs.  The
+// grid holds as many CTAs as fit on the SMs at once (their shared-memory rings set the
+// count); each loops over rows r = blockIdx.x + i * gridDim.x.  For each row one thread
 // issues a bulk global->shared copy (cp.async.bulk, the non-tensor form of TMA) of the
 // N partial rows and the residual row into stage i % S and arms the stage's mbarrier with
-// the byte count; while the CTA works on row i, rows i+1 .. i+S-1 are in flight.  A stage
+// the byte count; while the CTA works on row i, rows i+1 .. i+S-1 are in flight (with
+// S = 1 the next row's copy is issued as soon as the current row's square-sum is known and
+// overlaps the rest of its work, and other CTAs on the SM fill the gaps).  A stage
 // is refilled as soon as the row's square-sum has been reduced (by then every thread has
 // read its packs), so loads for later rows overlap the normalisation and the stores.
 // The weight packs a thread needs never change across rows and live in registers.
@@ -25,7 +28,7 @@
 namespace ar {
 
 struct StagedParams {
-  int stages;             // S, 2..4
+  int stages;             // S, 1..4
   int row_bytes;          // h * 2
   int* err;               // device status word (0 = fine), written only on a timeout
   long long wait_cycles;  // bound of one mbarrier wait

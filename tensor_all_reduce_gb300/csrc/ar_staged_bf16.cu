@@ -7,6 +7,7 @@ namespace ar {
 template <int N, bool Q>
 static const void* pick_staged_ppt_bf16(int ppt) {
   switch (ppt) {
+    case 1: return (const void*)&fused_staged_kernel<kBF16, N, 1, Q>;
     case 2: return (const void*)&fused_staged_kernel<kBF16, N, 2, Q>;
     case 4: return (const void*)&fused_staged_kernel<kBF16, N, 4, Q>;
     default: return nullptr;

@@ -53,6 +53,9 @@ def test_null_context_queries(lib):
     assert lib.ar_destroy(None) == tar.AR_OK
     assert tar.ar_last_variant(None) == ""
     assert lib.ar_init(None, 0, 0) == tar.AR_ERR_INVALID_ARG
+    code = ctypes.c_int(-1)
+    assert lib.ar_device_status(None, ctypes.byref(code)) == tar.AR_ERR_NOT_INITIALIZED
+    assert lib.ar_device_status(None, None) == tar.AR_ERR_INVALID_ARG
 
 
 BASE = 1 << 40   # fake, well-aligned device addresses; never dereferenced
