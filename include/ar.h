@@ -153,6 +153,37 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* args, void* 
  */
 ar_status ar_device_status(ar_ctx* ctx, int* code);
 
+/*
+ * Allocation-free form of ar_fused_reduce_rmsnorm, for callers that cannot call
+ * cudaMalloc where they need this op: an engine that has handed all device memory to a
+ * fixed plan (weights, KV cache, activations) up front, code running inside a stream
+ * capture (allocation is not allowed there in the global capture mode), or a loop that
+ * must not let an allocation synchronise the device.  Such callers cannot create a
+ * context, because ar_init allocates the staged kernel's status word; this entry point
+ * takes no context.  There is no counterpart on the pages.
+ *
+ * It runs the staged kernel only: arguments follow ar_fused_reduce_rmsnorm's rules, and
+ * in addition h must be a multiple of 8 and at most 8192 and every pointer 16-byte
+ * aligned (8-byte for q_out); otherwise it returns AR_ERR_UNSUPPORTED without launching.
+ * The device is the calling thread's current device.
+ *
+ * Scratch: the kernel's one status word lives in a static device array of
+ * AR_NOALLOC_SCRATCH_BYTES bytes inside the library, which every GPU that loads the
+ * library holds until the process exits.  A call whose scratch need exceeded that size
+ * would be refused with AR_ERR_UNSUPPORTED; the staged kernel needs 4 bytes at any size.
+ * Every call clears the word on `stream` before its launch (a cudaMemsetAsync, which
+ * allocates nothing).  All calls share the array, so calls that overlap on the GPU
+ * (different streams without ordering) race on it; a bounded wait that runs out (about a
+ * second) leaves incomplete outputs and code 1 in that word, which this interface does not
+ * read back.
+ *
+ * The first call on a device does a one-time set-up (device attributes, the kernels'
+ * shared-memory limit and the array's device address via cudaGetSymbolAddress); make that
+ * first call before any stream capture.  Later calls launch one memset and one kernel.
+ */
+#define AR_NOALLOC_SCRATCH_BYTES 256
+ar_status ar_fused_reduce_rmsnorm_noalloc(const ar_fused_args* args, void* stream);
+
 /* Static description of a status code. */
 const char* ar_status_string(ar_status s);
 
