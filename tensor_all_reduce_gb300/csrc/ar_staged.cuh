@@ -19,8 +19,8 @@
 // barrier sits outside any per-thread predicate.
 //
 // Waits are bounded: a wait on a stage's mbarrier gives up after `wait_cycles` SM clock
-// cycles, the CTA agrees on the failure with __syncthreads_or, records code 1 in
-// `err`, waits (bounded again) for its own copies still in flight, and returns.
+// cycles, the CTA agrees on the failure with __syncthreads_or, records code 1 in `err`,
+// waits (bounded again) for its own copies still in flight, and returns.
 #pragma once
 
 #include "ar_common.cuh"
@@ -127,21 +127,28 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
     for (int64_t i = 0; i < pre; ++i) issue((int)i, first + i * stride);
   }
 
-  // this thread's packs (fixed across rows) and their weights
+  // this thread's packs (fixed across rows) and their weight factors w' = w or 1 + w,
+  // computed once: they are the same for every row
   bool valid[PPT];
-  uint4 wpk[PPT];
+  float wv[PPT][8];
 #pragma unroll
   for (int k = 0; k < PPT; ++k) {
     const int pk = (int)threadIdx.x + k * (int)blockDim.x;
     valid[k] = pk < p.row_packs;
     const int pkc = valid[k] ? pk : 0;
-    wpk[k] = ld_keep(static_cast<const uint16_t*>(p.w) + (int64_t)pkc * 8);
+    unpack8<DT>(ld_keep(static_cast<const uint16_t*>(p.w) + (int64_t)pkc * 8), wv[k]);
+    if (p.gemma) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) wv[k][e] = 1.0f + wv[k][e];
+    }
   }
 
   for (int64_t i = 0; i < my_rows; ++i) {
     const int s = (int)(i % S);
     const uint32_t parity = (uint32_t)((i / S) & 1);
     const int64_t row = first + i * stride;
+    // Every thread waits on the stage's barrier itself (measured faster than one thread
+    // polling and a CTA barrier) and so observes the copy's completion before its reads.
     const bool ok = mbar_wait_bounded(&full_bar[s], parity, sp.wait_cycles);
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) atomicExch(sp.err, 1);
@@ -153,7 +160,8 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
     const uint8_t* st = stage_mem + (size_t)s * stage_bytes;
     const int64_t row_e = row * (int64_t)p.h;
 
-    uint4 z[PPT];
+    uint4 z[PPT];      // rounded residual sum, packed (stored as residual_out)
+    float zf[PPT][8];  // the same values as floats
     float ss = 0.0f;
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
@@ -178,11 +186,10 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
         sv = pack8<DT>(sf);
       }
       z[k] = sv;
+      unpack8<DT>(sv, zf[k]);
       if (valid[k]) {
-        float zf[8];
-        unpack8<DT>(sv, zf);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(zf[e], zf[e], ss);
+        for (int e = 0; e < 8; ++e) ss = fmaf(zf[k][e], zf[k][e], ss);
       }
     }
     const float tot = block_allreduce<false>(ss, red_ss[i & 1]);
@@ -201,20 +208,16 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
     float amax = 0.0f;
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
-      float zf[8], wf[8], yf[8];
-      unpack8<DT>(z[k], zf);
-      unpack8<DT>(wpk[k], wf);
+      float yf[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float wv = p.gemma ? 1.0f + wf[e] : wf[e];
-        yf[e] = (zf[e] * inv) * wv;
-      }
+      for (int e = 0; e < 8; ++e) yf[e] = (zf[k][e] * inv) * wv[k][e];
       y[k] = pack8<DT>(yf);
-      if (QUANT && valid[k]) {
-        float yr[8];
-        unpack8<DT>(y[k], yr);
+      if (QUANT) {
+        unpack8<DT>(y[k], zf[k]);  // zf now holds the ROUNDED output y
+        if (valid[k]) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(yr[e]));
+          for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(zf[k][e]));
+        }
       }
     }
     if (p.out != nullptr) {
@@ -230,13 +233,11 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
 #pragma unroll
       for (int k = 0; k < PPT; ++k) {
         if (!valid[k]) continue;
-        float yr[8];
-        unpack8<DT>(y[k], yr);
         uint32_t c[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float a = am == 0.0f ? 0.0f : div_rn_by(yr[2 * e], scale, rcp);
-          const float b = am == 0.0f ? 0.0f : div_rn_by(yr[2 * e + 1], scale, rcp);
+          const float a = am == 0.0f ? 0.0f : div_rn_by(zf[k][2 * e], scale, rcp);
+          const float b = am == 0.0f ? 0.0f : div_rn_by(zf[k][2 * e + 1], scale, rcp);
           c[e] = e4m3x2(a, b);
         }
         st_v2(p.q + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8,
