@@ -495,10 +495,10 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   } else if (ctx->force_variant == 1) {
     csize = 1;
   } else {
-    // spread small batches over the SMs: grow the cluster while fewer than two CTAs per
-    // SM would be launched and every CTA keeps at least 32 packs (256 elements)
+    // spread small batches over the SMs: grow the cluster while fewer CTAs than SMs would
+    // be launched and every CTA keeps at least 32 packs (256 elements)
     csize = 1;
-    const int64_t target = 2LL * ctx->sm_count;
+    const int64_t target = ctx->sm_count;
     while (csize < max_cl && a->m * csize < target && row_packs / (csize * 2) >= 32) csize *= 2;
     if (ctx->force_variant == 2 && csize == 1) csize = 2;
   }
