@@ -195,14 +195,18 @@ const char* ar_last_error(const ar_ctx* ctx);
  * "fused_staged", "fused_scalar", "fused_cluster_scalar" or "none" (empty call). */
 const char* ar_last_variant(const ar_ctx* ctx);
 
-/* Tuning and test overrides (0 = automatic for each).  Values outside the documented
- * range return AR_ERR_INVALID_ARG. */
+/* Tuning and test overrides (0 = automatic for each, except AR_OPT_PDL).  Values outside
+ * the documented range return AR_ERR_INVALID_ARG. */
 typedef enum {
   AR_OPT_FORCE_VARIANT = 0,  /* 0 auto, 1 row, 2 cluster, 3 staged, 4 scalar (tail) */
   AR_OPT_CLUSTER_SIZE = 1,   /* 0 auto, else 1, 2, 4, 8 or 16 CTAs per row */
   AR_OPT_PACKS_PER_THREAD = 2, /* 0 auto, else 1, 2 or 4 16-byte packs per thread */
   AR_OPT_REDUCE_UNROLL = 3,  /* 0 auto, else 1, 2 or 4 packs per thread per tile */
-  AR_OPT_STAGES = 4          /* 0 auto, else 1..4 shared-memory stages per CTA (staged variant) */
+  AR_OPT_STAGES = 4,         /* 0 auto, else 1..4 shared-memory stages per CTA (staged variant) */
+  AR_OPT_PDL = 5             /* 1 (the default): launch with programmatic dependent launch, so
+                                a kernel may be scheduled while its predecessor on the stream
+                                still runs (every kernel here waits for its predecessors to
+                                complete before it reads memory); 0: ordinary stream order */
 } ar_option;
 ar_status ar_set_option(ar_ctx* ctx, ar_option opt, int64_t value);
 

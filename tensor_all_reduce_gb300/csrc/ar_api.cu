@@ -27,6 +27,7 @@ struct ar_ctx {
   int ppt;
   int reduce_unroll;
   int stages;
+  int pdl;               // launch with programmatic stream serialisation
   const char* last_variant;
   char last_error[256];
 };
@@ -72,15 +73,22 @@ ar_status launch(ar_ctx* ctx, const void* fn, unsigned grid, unsigned block, int
   cfg.blockDim = dim3(block, 1, 1);
   cfg.dynamicSmemBytes = dyn_smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  unsigned na = 0;
   if (csize > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)csize;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)csize;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  if (ctx->pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
   cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
   if (e != cudaSuccess) return fail_cuda(ctx, e, "kernel launch");
   return AR_OK;
@@ -158,6 +166,7 @@ ar_status ar_init(ar_ctx** out, int device, unsigned flags) {
   ctx->l2_bytes = l2;
   ctx->last_variant = "none";
   ctx->max_cluster = 8;
+  ctx->pdl = 1;
 
   DeviceGuard g(device);
   // Load every kernel now (lazy module loading would otherwise do it on first launch,
@@ -278,6 +287,10 @@ ar_status ar_set_option(ar_ctx* ctx, ar_option opt, int64_t v) {
     case AR_OPT_STAGES:
       if (!(v == 0 || (v >= 1 && v <= 4))) return AR_ERR_INVALID_ARG;
       ctx->stages = (int)v;
+      return AR_OK;
+    case AR_OPT_PDL:
+      if (v != 0 && v != 1) return AR_ERR_INVALID_ARG;
+      ctx->pdl = (int)v;
       return AR_OK;
   }
   return AR_ERR_INVALID_ARG;

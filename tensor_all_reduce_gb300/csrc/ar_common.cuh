@@ -45,6 +45,22 @@ struct FusedParams {
 };
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// Every kernel starts with these two.  griddepcontrol.wait blocks until the grids this
+// one depends on (the previous kernels on the stream) have completed and their memory is
+// visible, so it must precede the first global read; it returns at once when the launch
+// carried no programmatic dependency.  griddepcontrol.launch_dependents then lets the next
+// kernel on the stream be scheduled early (once every CTA of this grid has started), so
+// its launch latency overlaps this grid's work; the next kernel does its own wait before
+// touching memory.
+__device__ __forceinline__ void pdl_wait_and_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // memory access
 // ---------------------------------------------------------------------------
 

@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
   __shared__ float red_amax[32];
   __shared__ float slot_ss, slot_amax, bcast;
 
+  pdl_wait_and_release();
   const int csize = p.csize;
   const int crank = (int)(blockIdx.x % (unsigned)csize);  // == %cluster_ctarank for (csize,1,1) clusters
   const int64_t row = blockIdx.x / (unsigned)csize;

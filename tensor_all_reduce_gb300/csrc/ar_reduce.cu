@@ -78,6 +78,7 @@ __device__ __forceinline__ void reduce_one_elem(const ReduceParams& p, int64_t e
 
 template <int DT, int N, int UNROLL, bool HAS_TAIL>
 __global__ void __launch_bounds__(256) reduce_vec_kernel(const ReduceParams p) {
+  pdl_wait_and_release();
   const int64_t bs = blockDim.x;
   const int64_t tile = bs * UNROLL;
   uint4* out = static_cast<uint4*>(p.out);
@@ -106,6 +107,7 @@ __global__ void __launch_bounds__(256) reduce_vec_kernel(const ReduceParams p) {
 // Element-wise form for pointers that are not 16-byte aligned.
 template <int DT, int N>
 __global__ void __launch_bounds__(256) reduce_scalar_kernel(const ReduceParams p) {
+  pdl_wait_and_release();
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < p.numel; e += stride)
     reduce_one_elem<DT, N>(p, e);

@@ -112,6 +112,7 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
     mbar_fence_init();
   }
   __syncthreads();
+  pdl_wait_and_release();
 
   auto issue = [&](int s, int64_t row) {
     uint8_t* dst = stage_mem + (size_t)s * stage_bytes;

@@ -48,6 +48,7 @@ def _reset_options(request):
         for opt in (tar.AR_OPT_FORCE_VARIANT, tar.AR_OPT_CLUSTER_SIZE, tar.AR_OPT_PACKS_PER_THREAD,
                     tar.AR_OPT_REDUCE_UNROLL, tar.AR_OPT_STAGES):
             c.set_option(opt, 0)
+        c.set_option(tar.AR_OPT_PDL, 1)
 
 
 # ---------------------------------------------------------------------------
