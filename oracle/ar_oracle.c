@@ -209,10 +209,12 @@ int orc_reduce_sum(void* out, const void* const* partials, int n, int64_t numel,
 /* step 2: residual add + RMSNorm (the unfused rmsnorm2d_fwd_with_add)      */
 /* ---------------------------------------------------------------------- */
 
-/* One row.  z_row receives the rounded residual sum as 16-bit bits. */
-static void add_rmsnorm_row(void* y, void* res_out, uint16_t* z_row, const void* s,
-                            const void* res_in, const void* w, int64_t row, int64_t h, float eps,
-                            int gemma, int dtype) {
+/* One row.  z_row receives the rounded residual sum as 16-bit bits.  With y32 non-NULL
+ * the normalised row is also written as binary32 (one rounding of the binary64 value);
+ * with skip_norm the output is z itself (no normalisation, weight unused). */
+static void add_rmsnorm_row_ex(void* y, float* y32, void* res_out, uint16_t* z_row, const void* s,
+                               const void* res_in, const void* w, int64_t row, int64_t h, float eps,
+                               int gemma, int skip_norm, int dtype) {
   int64_t base = row * h;
   for (int64_t j = 0; j < h; ++j) {
     float sv = load_elem(s, base + j, dtype);
@@ -224,7 +226,14 @@ static void add_rmsnorm_row(void* y, void* res_out, uint16_t* z_row, const void*
     }
     if (res_out) ((uint16_t*)res_out)[base + j] = z_row[j];
   }
-  if (!y) return;
+  if (!y && !y32) return;
+  if (skip_norm) {
+    for (int64_t j = 0; j < h; ++j) {
+      if (y) ((uint16_t*)y)[base + j] = z_row[j];
+      if (y32) y32[base + j] = load_elem(z_row, j, dtype);
+    }
+    return;
+  }
   double sumsq = 0.0;
   for (int64_t j = 0; j < h; ++j) {
     double zv = (double)load_elem(z_row, j, dtype);
@@ -236,8 +245,15 @@ static void add_rmsnorm_row(void* y, void* res_out, uint16_t* z_row, const void*
     double zv = (double)load_elem(z_row, j, dtype);
     double wv = (double)load_elem(w, j, dtype);
     double factor = gemma ? 1.0 + wv : wv;
-    store_elem_f64(y, base + j, zv * inv_rms * factor, dtype);
+    double yv = zv * inv_rms * factor;
+    if (y) store_elem_f64(y, base + j, yv, dtype);
+    if (y32) y32[base + j] = (float)yv;
   }
+}
+
+static void add_rmsnorm_row(void* y, void* res_out, uint16_t* z_row, const void* s, const void* res_in,
+                            const void* w, int64_t row, int64_t h, float eps, int gemma, int dtype) {
+  add_rmsnorm_row_ex(y, NULL, res_out, z_row, s, res_in, w, row, h, eps, gemma, 0, dtype);
 }
 
 int orc_add_rmsnorm(void* y, void* res_out, const void* s, const void* res_in, const void* w,
@@ -288,10 +304,16 @@ int orc_per_token_quant(uint8_t* q, float* scale, const void* y, int64_t m, int6
 int orc_fused_reduce_rmsnorm(void* y, void* res_out, uint8_t* q, float* scale,
                              const void* const* partials, int n, const void* res_in, const void* w,
                              int64_t m, int64_t h, float eps, int gemma, int quant, int dtype) {
-  if (!partials || n < 1 || !w || m < 0 || h < 1) return -1;
+  return orc_fused_ex(y, NULL, res_out, q, scale, partials, n, res_in, w, m, h, eps, gemma, quant, 0, dtype);
+}
+
+int orc_fused_ex(void* y, float* y32, void* res_out, uint8_t* q, float* scale, const void* const* partials,
+                 int n, const void* res_in, const void* w, int64_t m, int64_t h, float eps, int gemma,
+                 int quant, int skip_norm, int dtype) {
+  if (!partials || n < 1 || (!w && !skip_norm) || m < 0 || h < 1) return -1;
   if (dtype != ORC_F16 && dtype != ORC_BF16) return -1;
   if (quant && (!q || !scale)) return -1;
-  if (!quant && !y) return -1;
+  if (!quant && !y && !y32) return -1;
   for (int r = 0; r < n; ++r)
     if (!partials[r]) return -1;
 
@@ -310,7 +332,8 @@ int orc_fused_reduce_rmsnorm(void* y, void* res_out, uint8_t* q, float* scale,
     for (int k = 0; k < n; ++k) row_ptrs[k] = (const uint16_t*)partials[k] + base;
     orc_reduce_sum(s_row, row_ptrs, n, h, dtype);
     const void* res_row = res_in ? (const void*)((const uint16_t*)res_in + base) : NULL;
-    add_rmsnorm_row(y_row, ro_row, z_row, s_row, res_row, w, 0, h, eps, gemma, dtype);
+    add_rmsnorm_row_ex(y_row, y32 ? y32 + base : NULL, ro_row, z_row, s_row, res_row, w, 0, h, eps, gemma,
+                       skip_norm, dtype);
     if (res_out) memcpy((uint16_t*)res_out + base, ro_row, row_bytes);
     if (y) memcpy((uint16_t*)y + base, y_row, row_bytes);
     if (quant) quant_row(q + base, scale + r, y_row, 0, h, dtype);

@@ -85,6 +85,16 @@ int orc_fused_reduce_rmsnorm(void* y, void* res_out, uint8_t* q, float* scale,
                              const void* const* partials, int n, const void* res_in, const void* w,
                              int64_t m, int64_t h, float eps, int gemma, int quant, int dtype);
 
+/* The whole path with its two options.
+ *   y32 (may be NULL): the normalised row as binary32, RN_f32 of the binary64 value
+ *       z * inv * w' (no rounding to the 16-bit type first);
+ *   skip_norm: no normalisation, the output is z itself (the rounded sum plus residual);
+ *       w may then be NULL and eps, gemma are unused.
+ * The FP8 epilogue always quantises the 16-bit output (z with skip_norm). */
+int orc_fused_ex(void* y, float* y32, void* res_out, uint8_t* q, float* scale, const void* const* partials,
+                 int n, const void* res_in, const void* w, int64_t m, int64_t h, float eps, int gemma,
+                 int quant, int skip_norm, int dtype);
+
 #ifdef __cplusplus
 }
 #endif

@@ -293,3 +293,64 @@ def test_quant_properties(orc, dtype):
     assert np.array_equal(scn, sc)
     nz = q != 0
     assert np.array_equal(qn[nz], q[nz] ^ np.uint8(0x80))
+
+
+# ---------------------------------------------------------------------------
+# options: no normalisation (all-reduce + per-token FP8) and binary32 output
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_skip_norm_is_the_rounded_residual_sum(orc, dtype):
+    inp = synth.fused_inputs(4, 9, 300, dtype, seed=31)
+    ps = [synth.bits(p) for p in inp["partials"]]
+    res = synth.bits(inp["residual"])
+    out = orc.fused_ex(ps, res, None, 0.0, False, True, dtype, skip_norm=True, out_fp32=True)
+    assert np.array_equal(out["y"], out["res_out"])
+    # y32 holds exactly the 16-bit values
+    assert np.array_equal(out["y32"], _dec(out["res_out"], dtype))
+    s = orc.reduce_sum(ps, dtype)
+    _, z = orc.add_rmsnorm(s, res, synth.bits(inp["weight"]), 1e-6, False, dtype)
+    assert np.array_equal(out["res_out"], z)
+    q, sc = orc.per_token_quant(z, dtype)
+    assert np.array_equal(out["q"], q) and np.array_equal(out["scale"], sc)
+    # no residual: the output is the reduced sum itself
+    out2 = orc.fused_ex(ps, None, None, 0.0, False, False, dtype, skip_norm=True)
+    assert np.array_equal(out2["y"], s)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("gemma", [False, True])
+def test_fp32_output_is_nearest_binary32_of_exact_value(orc, dtype, gemma):
+    getcontext().prec = 60
+    g = torch.Generator().manual_seed(17)
+    for h in (1, 3, 8, 21):
+        ps = [torch.randn((2, h), generator=g).to(TDT[dtype]) for _ in range(3)]
+        res = torch.randn((2, h), generator=g).to(TDT[dtype])
+        w = (0.3 * torch.randn((h,), generator=g) + (0.0 if gemma else 1.0)).to(TDT[dtype])
+        out = orc.fused_ex([synth.bits(p) for p in ps], synth.bits(res), synth.bits(w), 1e-6, gemma, False,
+                           dtype, out_fp32=True)
+        z = _dec(out["res_out"], dtype).astype(np.float64)
+        wf = _dec(synth.bits(w), dtype).astype(np.float64)
+        y32 = out["y32"]
+        e32 = Fraction(float(np.float32(1e-6)))
+        for r in range(2):
+            ms = sum(Fraction(float(v)) ** 2 for v in z[r]) / h + e32
+            root = Decimal(ms.numerator).sqrt() / Decimal(ms.denominator).sqrt()
+            for j in range(h):
+                num = Fraction(float(z[r, j])) * (Fraction(float(wf[j])) + (1 if gemma else 0))
+                exact = Decimal(num.numerator) / Decimal(num.denominator) / root
+                got = Decimal(float(y32[r, j]))
+                for nb in (np.nextafter(y32[r, j], np.float32(np.inf)), np.nextafter(y32[r, j], np.float32(-np.inf))):
+                    assert abs(got - exact) <= abs(Decimal(float(nb)) - exact) + abs(exact) * Decimal(2) ** -45
+        # the 16-bit output is within one 16-bit ulp of the binary32 one
+        y = _dec(out["y"], dtype).astype(np.float64)
+        assert np.all(np.abs(y - y32) <= np.abs(y32) * (2.0 ** -8 if dtype == "bf16" else 2.0 ** -11) + 1e-30)
+
+
+def test_fp32_output_closed_forms(orc):
+    one = _t([1.0] * 4, "bf16")
+    s = _t([[3.0] * 4, [2.0, 0.0, 0.0, 0.0]], "bf16")
+    out = orc.fused_ex([s], None, one, 0.0, False, False, "bf16", out_fp32=True)
+    assert list(out["y32"][0]) == [1.0] * 4
+    assert list(out["y32"][1]) == [2.0, 0.0, 0.0, 0.0]
+

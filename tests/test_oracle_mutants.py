@@ -43,8 +43,15 @@ MUTANTS = [
      "if (a >= 464.0) return (uint8_t)(sign | 0x7Fu);"),
     ("bf16_bias", "encode_fields(r, 8, -126, 127)", "encode_fields(r, 8, -126, 126)"),
     ("f16_max_finite_overflows", "if (r >= 65536.0)", "if (r >= 65504.0)"),
-    ("row_stride", "static void add_rmsnorm_row(void* y, void* res_out, uint16_t* z_row, const void* s,\n                            const void* res_in, const void* w, int64_t row, int64_t h, float eps,\n                            int gemma, int dtype) {\n  int64_t base = row * h;",
-     "static void add_rmsnorm_row(void* y, void* res_out, uint16_t* z_row, const void* s,\n                            const void* res_in, const void* w, int64_t row, int64_t h, float eps,\n                            int gemma, int dtype) {\n  int64_t base = row * (h > 1 ? h - 1 : 1);"),
+    ("row_stride", "int gemma, int skip_norm, int dtype) {\n  int64_t base = row * h;",
+     "int gemma, int skip_norm, int dtype) {\n  int64_t base = row * (h > 1 ? h - 1 : 1);"),
+    ("fp32_output_drops_weight", "if (y32) y32[base + j] = (float)yv;",
+     "if (y32) y32[base + j] = (float)(zv * inv_rms);"),
+    ("fp32_output_via_16bit", "if (y32) y32[base + j] = (float)yv;",
+     "if (y32) y32[base + j] = (float)zv * (float)inv_rms * (float)factor;"),
+    ("skip_norm_outputs_the_sum", "if (y32) y32[base + j] = load_elem(z_row, j, dtype);",
+     "if (y32) y32[base + j] = load_elem(s, base + j, dtype);"),
+    ("skip_norm_still_normalises", "  if (skip_norm) {\n", "  if (0) {\n"),
 ]
 
 
