@@ -185,7 +185,7 @@ class FusedSets:
         self.res = torch.empty((sets, m, h), dtype=t, device=dev) if wl.residual else None
         self.w = inp["weight"].to(dev)
         want_y = wl.mirror or not wl.quant
-        self.out = torch.empty((sets, m, h), dtype=t, device=dev) if want_y else None
+        self.out = torch.empty((sets, m, h), dtype=torch.float32 if wl.out_fp32 else t, device=dev) if want_y else None
         self.ro = torch.empty((sets, m, h), dtype=t, device=dev) if wl.residual else None
         self.q = torch.empty((sets, m, h), dtype=torch.uint8, device=dev) if wl.quant else None
         self.sc = torch.empty((sets, m), dtype=torch.float32, device=dev) if wl.quant else None
@@ -203,7 +203,8 @@ class FusedSets:
                                  residual_out=None if self.ro is None else self.ro[r],
                                  q_out=None if self.q is None else self.q[r],
                                  scale_out=None if self.sc is None else self.sc[r],
-                                 want_out=self.out is not None, want_residual_out=self.ro is not None)
+                                 want_out=self.out is not None, want_residual_out=self.ro is not None,
+                                 skip_norm=wl.skip_norm, out_fp32=wl.out_fp32)
 
 
 class ReduceSets:
@@ -369,7 +370,7 @@ def sweep(ctx, dev, l2, peak):
     import torch
     from tensor_all_reduce_gb300 import synth
     out = []
-    for wl in synth.all_fused() + synth.reduce_only():
+    for wl in synth.all_fused() + synth.options() + synth.reduce_only():
         fused = isinstance(wl, synth.FusedWorkload)
         fp = wl.algorithmic_bytes()
         R = rotation_sets(fp, l2)

@@ -114,7 +114,7 @@ typedef struct {
   const void* partials[AR_MAX_PARTIALS];   /* device, [m, h] of dtype each */
   const void* residual_in;                 /* device [m, h] or NULL (then z = s) */
   void* residual_out;                      /* device [m, h] or NULL */
-  const void* weight;                      /* device [h] of dtype, required */
+  const void* weight;                      /* device [h] of dtype, required unless skip_norm */
   void* out;                               /* device [m, h]: y (the bf16/fp16 "mirror" when quant is on);
                                               NULL allowed only when quant is on */
   float eps;                               /* finite, >= 0 */
@@ -126,6 +126,13 @@ typedef struct {
                                               only weight must be non-NULL) */
   int64_t h;                               /* hidden size, >= 1 */
   ar_dtype dtype;                          /* AR_DTYPE_BF16 or AR_DTYPE_F16 */
+  int skip_norm;                           /* != 0: no RMSNorm; the output is z (the rounded sum plus
+                                              residual), the FP8 epilogue quantises z (all-reduce +
+                                              dynamic per-token FP8); weight may be NULL, eps and
+                                              gemma are ignored */
+  int out_fp32;                            /* != 0: `out` is [m, h] fp32 and receives the normalised
+                                              row before its rounding to dtype (the FP8 epilogue still
+                                              quantises the dtype-rounded row) */
 } ar_fused_args;
 
 /*

@@ -62,6 +62,8 @@ class ArFusedArgs(ctypes.Structure):
         ("m", ctypes.c_int64),
         ("h", ctypes.c_int64),
         ("dtype", ctypes.c_int),
+        ("skip_norm", ctypes.c_int),
+        ("out_fp32", ctypes.c_int),
     ]
 
 
@@ -184,8 +186,9 @@ def ar_fused_reduce_rmsnorm(ctx: int, args: ArFusedArgs, stream: Optional[int] =
 
 
 def make_fused_args(partials: Sequence[int], residual_in: Optional[int], residual_out: Optional[int],
-                    weight: int, out: Optional[int], eps: float, gemma: bool, quant: bool,
-                    q_out: Optional[int], scale_out: Optional[int], m: int, h: int, dtype: int) -> ArFusedArgs:
+                    weight: Optional[int], out: Optional[int], eps: float, gemma: bool, quant: bool,
+                    q_out: Optional[int], scale_out: Optional[int], m: int, h: int, dtype: int,
+                    skip_norm: bool = False, out_fp32: bool = False) -> ArFusedArgs:
     a = ArFusedArgs()
     a.n = len(partials)
     for i, p in enumerate(partials):
@@ -202,6 +205,8 @@ def make_fused_args(partials: Sequence[int], residual_in: Optional[int], residua
     a.m = m
     a.h = h
     a.dtype = dtype
+    a.skip_norm = int(bool(skip_norm))
+    a.out_fp32 = int(bool(out_fp32))
     return a
 
 
@@ -275,8 +280,10 @@ class Context:
 
     def fused_reduce_rmsnorm(self, partials, residual, weight, eps: float = 1e-6, gemma: bool = False,
                              quant: bool = False, out=None, residual_out=None, q_out=None, scale_out=None,
-                             want_out: bool = True, want_residual_out: bool = True, stream=None):
-        """Returns (out, residual_out, q_out, scale_out); absent outputs are None."""
+                             want_out: bool = True, want_residual_out: bool = True, stream=None,
+                             skip_norm: bool = False, out_fp32: bool = False):
+        """Returns (out, residual_out, q_out, scale_out); absent outputs are None.  With
+        skip_norm there is no RMSNorm (weight may be None); with out_fp32 `out` is float32."""
         import torch
         x0 = partials[0]
         m, h = x0.shape
@@ -284,7 +291,7 @@ class Context:
             if p.shape != (m, h) or p.dtype != x0.dtype or not p.is_contiguous() or not p.is_cuda:
                 raise ValueError("partials and residual must be contiguous [m, h] CUDA tensors of one dtype")
         if out is None and (want_out or not quant):
-            out = torch.empty_like(x0)
+            out = torch.empty((m, h), dtype=torch.float32 if out_fp32 else x0.dtype, device=x0.device)
         if residual_out is None and want_residual_out:
             residual_out = torch.empty_like(x0)
         if quant:
@@ -293,7 +300,7 @@ class Context:
             if scale_out is None:
                 scale_out = torch.empty((m,), dtype=torch.float32, device=x0.device)
         args = make_fused_args([p.data_ptr() for p in partials], _ptr(residual), _ptr(residual_out),
-                               weight.data_ptr(), _ptr(out), eps, gemma, quant, _ptr(q_out), _ptr(scale_out),
-                               m, h, _torch_dtype_code(x0))
+                               _ptr(weight), _ptr(out), eps, gemma, quant, _ptr(q_out), _ptr(scale_out),
+                               m, h, _torch_dtype_code(x0), skip_norm=skip_norm, out_fp32=out_fp32)
         ar_fused_reduce_rmsnorm(self.handle, args, _stream(stream))
         return out, residual_out, q_out, scale_out

@@ -381,7 +381,8 @@ ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int
 
 ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* stream) {
   if (!a) return AR_ERR_INVALID_ARG;
-  if (a->n < 1 || a->n > AR_MAX_PARTIALS || a->m < 0 || a->h < 1 || !a->weight) return AR_ERR_INVALID_ARG;
+  if (a->n < 1 || a->n > AR_MAX_PARTIALS || a->m < 0 || a->h < 1 || (!a->weight && !a->skip_norm))
+    return AR_ERR_INVALID_ARG;
   if (a->dtype != AR_DTYPE_BF16 && a->dtype != AR_DTYPE_F16) return AR_ERR_INVALID_ARG;
   if (a->quant != AR_QUANT_NONE && a->quant != AR_QUANT_FP8_E4M3_PER_TOKEN) return AR_ERR_INVALID_ARG;
   const bool quant = a->quant == AR_QUANT_FP8_E4M3_PER_TOKEN;
@@ -398,13 +399,14 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
     if (!a->partials[r]) return AR_ERR_INVALID_ARG;
 
   const int es = elem_size(a->dtype);
+  const int oes = a->out_fp32 ? 4 : es;  // element size of `out`
   const int64_t mh = a->m * a->h;
   const int64_t tb = mh * es;  // bytes of one [m, h] tensor
   // element alignment
   for (int r = 0; r < a->n; ++r)
     if (!aligned(a->partials[r], es)) return AR_ERR_ALIGNMENT;
   if ((a->residual_in && !aligned(a->residual_in, es)) || (a->residual_out && !aligned(a->residual_out, es)) ||
-      !aligned(a->weight, es) || (a->out && !aligned(a->out, es)) || (quant && !aligned(a->scale_out, 4)))
+      !aligned(a->weight, es) || (a->out && !aligned(a->out, oes)) || (quant && !aligned(a->scale_out, 4)))
     return AR_ERR_ALIGNMENT;
   // overlap: outputs may equal an [m, h] input of the same type exactly (every element is
   // read before the same thread writes it), never partially overlap an input, and never
@@ -414,11 +416,11 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   int ni = 0;
   for (int r = 0; r < a->n; ++r) ins[ni++] = {a->partials[r], tb, true};
   if (a->residual_in) ins[ni++] = {a->residual_in, tb, true};
-  ins[ni++] = {a->weight, (int64_t)a->h * es, false};
+  if (a->weight) ins[ni++] = {a->weight, (int64_t)a->h * es, false};
   Range outs[4];
   int no = 0;
   if (a->residual_out) outs[no++] = {a->residual_out, tb, true};
-  if (a->out) outs[no++] = {a->out, tb, true};
+  if (a->out) outs[no++] = {a->out, mh * oes, !a->out_fp32};
   if (quant) {
     outs[no++] = {a->q_out, mh, false};
     outs[no++] = {a->scale_out, a->m * 4, false};
@@ -480,6 +482,8 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
     p.eps = a->eps;
     p.inv_h = (float)(1.0 / (double)a->h);
     p.gemma = a->gemma != 0;
+    p.skip_norm = a->skip_norm != 0;
+    p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
     ar::StagedParams sp;
     sp.stages = S;
     sp.row_bytes = (int)(a->h * es);
@@ -546,6 +550,8 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   p.eps = a->eps;
   p.inv_h = (float)(1.0 / (double)a->h);
   p.gemma = a->gemma != 0;
+  p.skip_norm = a->skip_norm != 0;
+  p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
 
   const void* fn = a->dtype == AR_DTYPE_BF16 ? ar::fused_kernel_bf16(a->n, ppt, quant, vec)
                                              : ar::fused_kernel_f16(a->n, ppt, quant, vec);

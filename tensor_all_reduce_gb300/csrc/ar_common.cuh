@@ -42,6 +42,8 @@ struct FusedParams {
   float eps;
   float inv_h;       // 1 / h
   int gemma;
+  int skip_norm;     // 1: no normalisation, y = z (weight unused)
+  int out_f32;       // 1: `out` holds fp32 values of y before their rounding
 };
 
 // ---------------------------------------------------------------------------

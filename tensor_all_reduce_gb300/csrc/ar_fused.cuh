@@ -57,6 +57,22 @@ __device__ __forceinline__ void store_pack(void* base, int64_t e0, int64_t limit
   }
 }
 
+// Store eight fp32 values (elements e0 .. e0+7 of an fp32 [m, h] array).
+template <bool VEC>
+__device__ __forceinline__ void store_f32x8(void* base, int64_t e0, int64_t limit, const float (&f)[8]) {
+  float* b = static_cast<float*>(base);
+  if constexpr (VEC) {
+    st_v4(b + e0, make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                             __float_as_uint(f[3])));
+    st_v4(b + e0 + 4, make_uint4(__float_as_uint(f[4]), __float_as_uint(f[5]), __float_as_uint(f[6]),
+                                 __float_as_uint(f[7])));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (e0 + i < limit) st_f32(b + e0 + i, f[i]);
+  }
+}
+
 template <int DT, int N, int PPT, bool QUANT, bool VEC>
 __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) {
   __shared__ float red_ss[32];
@@ -105,12 +121,14 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
       s = pack8<DT>(sf);                                   // second rounding to T
     }
     z[k] = s;
-    // weight row: 8 consecutive entries starting at column pkc * 8
-    {
+    // weight row: 8 consecutive entries starting at column pkc * 8 (none without the norm)
+    if (!p.skip_norm) {
       float wf[8];
       const int64_t c0 = (int64_t)pkc * 8;
       load_pack<DT, VEC, false>(p.w, c0, valid[k] ? (int64_t)p.h : 0, wf);
       wpk[k] = pack8<DT>(wf);                              // exact: wf are T values
+    } else {
+      wpk[k] = make_uint4(0, 0, 0, 0);
     }
     if (valid[k]) {
       float zf[8];
@@ -130,12 +148,15 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
   }
 
   // ---- row square-sum: warp -> block -> cluster ------------------------------------
-  float tot = block_allreduce<false>(ss, red_ss);
-  if (csize > 1) {
-    if (threadIdx.x == 0) slot_ss = tot;
-    tot = cluster_gather<false>(&slot_ss, &bcast, csize);
+  float inv = 1.0f;  // without the norm y = z * 1 * 1 = z exactly
+  if (!p.skip_norm) {
+    float tot = block_allreduce<false>(ss, red_ss);
+    if (csize > 1) {
+      if (threadIdx.x == 0) slot_ss = tot;
+      tot = cluster_gather<false>(&slot_ss, &bcast, csize);
+    }
+    inv = rsqrtf(tot * p.inv_h + p.eps);
   }
-  const float inv = rsqrtf(tot * p.inv_h + p.eps);
 
   // ---- phase 2: normalise, weight, round ---------------------------------------------
   uint4 y[PPT];
@@ -147,10 +168,14 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
     unpack8<DT>(wpk[k], wf);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-      const float wv = p.gemma ? 1.0f + wf[i] : wf[i];
+      const float wv = p.skip_norm ? 1.0f : (p.gemma ? 1.0f + wf[i] : wf[i]);
       yf[i] = (zf[i] * inv) * wv;
     }
     y[k] = pack8<DT>(yf);
+    if (p.out_f32 && valid[k]) {
+      const int pk = pk_begin + (int)threadIdx.x + k * (int)blockDim.x;
+      store_f32x8<VEC>(p.out, row_e + (int64_t)pk * 8, row_end, yf);
+    }
     if (QUANT && valid[k]) {
       float yr[8];
       unpack8<DT>(y[k], yr);                               // amax of the ROUNDED output
@@ -158,7 +183,7 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
       for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(yr[i]));
     }
   }
-  if (p.out != nullptr) {
+  if (p.out != nullptr && !p.out_f32) {
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
       if (valid[k]) {

@@ -129,6 +129,8 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_noalloc(const ar_fused_args* a, voi
   p.eps = a->eps;
   p.inv_h = (float)(1.0 / (double)a->h);
   p.gemma = a->gemma != 0;
+  p.skip_norm = a->skip_norm != 0;
+  p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
   ar::StagedParams sp;
   sp.stages = S;
   sp.row_bytes = (int)(a->h * es);

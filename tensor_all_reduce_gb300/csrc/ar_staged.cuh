@@ -137,10 +137,15 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
     const int pk = (int)threadIdx.x + k * (int)blockDim.x;
     valid[k] = pk < p.row_packs;
     const int pkc = valid[k] ? pk : 0;
-    unpack8<DT>(ld_keep(static_cast<const uint16_t*>(p.w) + (int64_t)pkc * 8), wv[k]);
-    if (p.gemma) {
+    if (p.skip_norm) {  // no norm: y = z * 1 * 1 = z exactly; the weight is not read
 #pragma unroll
-      for (int e = 0; e < 8; ++e) wv[k][e] = 1.0f + wv[k][e];
+      for (int e = 0; e < 8; ++e) wv[k][e] = 1.0f;
+    } else {
+      unpack8<DT>(ld_keep(static_cast<const uint16_t*>(p.w) + (int64_t)pkc * 8), wv[k]);
+      if (p.gemma) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) wv[k][e] = 1.0f + wv[k][e];
+      }
     }
   }
 
@@ -193,7 +198,11 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
         for (int e = 0; e < 8; ++e) ss = fmaf(zf[k][e], zf[k][e], ss);
       }
     }
-    const float tot = block_allreduce<false>(ss, red_ss[i & 1]);
+    float tot = 0.0f;
+    if (!p.skip_norm)
+      tot = block_allreduce<false>(ss, red_ss[i & 1]);
+    else
+      __syncthreads();
     // every thread has read stage s: refill it with the row S iterations ahead
     if (threadIdx.x == 0 && i + S < my_rows) {
       fence_proxy_async_smem();
@@ -204,7 +213,7 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
       for (int k = 0; k < PPT; ++k)
         if (valid[k]) st_v4(static_cast<uint16_t*>(p.res_out) + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8, z[k]);
     }
-    const float inv = rsqrtf(tot * p.inv_h + p.eps);
+    const float inv = p.skip_norm ? 1.0f : rsqrtf(tot * p.inv_h + p.eps);
     uint4 y[PPT];
     float amax = 0.0f;
 #pragma unroll
@@ -213,6 +222,13 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
 #pragma unroll
       for (int e = 0; e < 8; ++e) yf[e] = (zf[k][e] * inv) * wv[k][e];
       y[k] = pack8<DT>(yf);
+      if (p.out_f32 && valid[k]) {
+        float* o = static_cast<float*>(p.out) + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8;
+        st_v4(o, make_uint4(__float_as_uint(yf[0]), __float_as_uint(yf[1]), __float_as_uint(yf[2]),
+                            __float_as_uint(yf[3])));
+        st_v4(o + 4, make_uint4(__float_as_uint(yf[4]), __float_as_uint(yf[5]), __float_as_uint(yf[6]),
+                                __float_as_uint(yf[7])));
+      }
       if (QUANT) {
         unpack8<DT>(y[k], zf[k]);  // zf now holds the ROUNDED output y
         if (valid[k]) {
@@ -221,7 +237,7 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
         }
       }
     }
-    if (p.out != nullptr) {
+    if (p.out != nullptr && !p.out_f32) {
 #pragma unroll
       for (int k = 0; k < PPT; ++k)
         if (valid[k]) st_v4(static_cast<uint16_t*>(p.out) + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8, y[k]);

@@ -80,6 +80,8 @@ class FusedWorkload:
     mirror: bool = True          # write the normed output (the bf16 mirror when quant is on)
     residual: bool = True
     seed: int = 1234
+    skip_norm: bool = False      # all-reduce (+ residual) + per-token FP8 without RMSNorm
+    out_fp32: bool = False       # the normed output stored as fp32
 
     def inputs(self) -> Dict[str, object]:
         return fused_inputs(self.n, self.m, self.h, self.dtype, self.seed, self.gemma, self.residual)
@@ -89,11 +91,11 @@ class FusedWorkload:
         write, one weight read, the normed output, FP8 codes and per-row scales."""
         b = ELEM_SIZE[self.dtype]
         mh = self.m * self.h
-        total = self.n * mh * b + self.h * b
+        total = self.n * mh * b + (0 if self.skip_norm else self.h * b)
         if self.residual:
             total += 2 * mh * b
         if self.mirror or not self.quant:
-            total += mh * b
+            total += mh * (4 if self.out_fp32 else b)
         if self.quant:
             total += mh + 4 * self.m
         return total
@@ -139,12 +141,20 @@ def large_m() -> List[FusedWorkload]:
     return [FusedWorkload("n8_m4096_h6144_bf16_plain", 8, 4096, 6144, seed=1238)]
 
 
+def options() -> List[FusedWorkload]:
+    """The fused path's further forms: all-reduce + residual + per-token FP8 without the norm,
+    and the normalised output in fp32."""
+    return [FusedWorkload("n4_m2800_h6144_bf16_nonorm_fp8", 4, 2800, 6144, quant=True, mirror=False,
+                          skip_norm=True, seed=1239),
+            FusedWorkload("n4_m2800_h6144_bf16_f32out", 4, 2800, 6144, out_fp32=True, seed=1240)]
+
+
 def all_fused() -> List[FusedWorkload]:
     return small_fused() + decode_sweep() + gemma_fp8() + large_m()
 
 
 def by_name(name: str):
-    for w in all_fused() + reduce_only():
+    for w in all_fused() + options() + reduce_only():
         if w.name == name:
             return w
     raise KeyError(name)

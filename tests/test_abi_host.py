@@ -126,7 +126,14 @@ def test_fused_validation(lib):
     assert fused(out=BASE + 7 * 64 * MB + 1) == AL
     assert fused(weight=BASE + 6 * 64 * MB + 1) == AL
     assert fused(quant=True, q_out=BASE + 8 * 64 * MB, scale_out=BASE + 9 * 64 * MB + 2) == AL
+    # without the norm the weight may be absent; with it, it may not
+    assert fused(weight=None, skip_norm=True) == NI
+    assert fused(weight=None, skip_norm=False) == IA
+    # fp32 output: 4-byte alignment, and never an alias of a 16-bit input
+    assert fused(out_fp32=True, out=BASE + 7 * 64 * MB + 2) == AL
+    assert fused(out_fp32=True, m=8) == NI
     OV = tar.AR_ERR_OVERLAP
+    assert fused(out_fp32=True, out=BASE) == OV                          # fp32 y over partials[0]
     assert fused(out=BASE + 32) == OV                                   # inside partials[0]
     assert fused(residual_out=BASE + 7 * 64 * MB) == OV                 # residual_out == out
     assert fused(out=BASE + 6 * 64 * MB) == OV                          # out on the weight
