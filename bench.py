@@ -207,6 +207,31 @@ class FusedSets:
                                  skip_norm=wl.skip_norm, out_fp32=wl.out_fp32)
 
 
+class BatchSets:
+    """`k` independent calls of one fused workload per step, either as one batched launch or
+    as k separate launches, rotating over R sets of k buffer sets."""
+
+    def __init__(self, wl, k: int, sets: int, dev, batched: bool):
+        self.inner = FusedSets(wl, k * sets, dev)
+        self.k, self.R, self.batched = k, sets, batched
+
+    def call(self, ctx, i: int):
+        base = (i % self.R) * self.k
+        if not self.batched:
+            for j in range(self.k):
+                self.inner.call(ctx, base + j)
+            return
+        f, wl = self.inner, self.inner.wl
+        calls = []
+        for j in range(self.k):
+            r = base + j
+            calls.append({"partials": list(f.parts[r].unbind(0)), "residual": None if f.res is None else f.res[r],
+                          "weight": f.w, "eps": 1e-6, "gemma": wl.gemma, "quant": wl.quant,
+                          "out": None if f.out is None else f.out[r], "residual_out": None if f.ro is None else f.ro[r],
+                          "q_out": None if f.q is None else f.q[r], "scale_out": None if f.sc is None else f.sc[r]})
+        ctx.fused_reduce_rmsnorm_batch(calls)
+
+
 class ReduceSets:
     def __init__(self, wl, sets: int, dev):
         import torch
@@ -390,6 +415,24 @@ def sweep(ctx, dev, l2, peak):
         out.append({"workload": wl.name, "variant": variant, "us_per_call_cold": round(cold, 3),
                     "us_per_call_l2_warm": round(warm, 3), "bytes_per_call": fp, "gbs_cold": round(gbs, 1),
                     "frac_of_peak_cold": round(gbs / peak, 4), "rotation_sets": R})
+    # 8 independent decode calls (16 x 6144 each): one batched launch against 8 launches
+    wl = synth.FusedWorkload("n4_m16_h6144_bf16_decode", 4, 16, 6144, seed=1236)
+    k = 8
+    R = rotation_sets(k * wl.algorithmic_bytes(), l2, cap=64)
+    for batched in (True, False):
+        sets = BatchSets(wl, k, R, dev, batched)
+        ms, _, _ = time_graph(sets, ctx, max(R, 32), steps=5, warmup=2, world=1)
+        cold = ms * 1000 / (5 * max(R, 32))
+        variant = ctx.last_variant
+        del sets
+        sets = BatchSets(wl, k, 1, dev, batched)
+        ms, _, _ = time_graph(sets, ctx, 32, steps=5, warmup=2, world=1)
+        warm = ms * 1000 / (5 * 32)
+        del sets
+        torch.cuda.empty_cache()
+        out.append({"workload": f"{k}x_{wl.name}_{'batched' if batched else 'separate'}", "variant": variant,
+                    "us_per_call_cold": round(cold, 3), "us_per_call_l2_warm": round(warm, 3),
+                    "bytes_per_call": k * wl.algorithmic_bytes(), "unit_note": "one step = 8 calls", "rotation_sets": R})
     return out
 
 

@@ -161,6 +161,23 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* args, void* 
 ar_status ar_device_status(ar_ctx* ctx, int* code);
 
 /*
+ * Several independent fused calls in one launch, so a batch of decode-sized calls pays
+ * one launch instead of `count` (SURVEY-ranked follow-up of the interleaved small and
+ * large fused calls on [P1] Changes).
+ *
+ * calls: host array of `count` (1..AR_MAX_BATCH) argument blocks, each valid for
+ * ar_fused_reduce_rmsnorm on its own and all with the same n, dtype, quant, skip_norm and
+ * out_fp32.  The calls run concurrently, so no call may write memory that another call
+ * reads or writes (AR_ERR_OVERLAP); inputs may be shared (for example one weight).  When
+ * every call has 16-byte-aligned rows of at most 8192 elements (h a multiple of 8) this is
+ * one kernel with one CTA per row of every call; otherwise the calls are launched one
+ * after another (same results).  Results equal those of the separate calls within the
+ * single-call bars (residual_out and FP8 from the same y bit-exact, y within one ulp).
+ */
+#define AR_MAX_BATCH 16
+ar_status ar_fused_reduce_rmsnorm_batch(ar_ctx* ctx, const ar_fused_args* calls, int count, void* stream);
+
+/*
  * Allocation-free form of ar_fused_reduce_rmsnorm, for callers that cannot call
  * cudaMalloc where they need this op: an engine that has handed all device memory to a
  * fixed plan (weights, KV cache, activations) up front, code running inside a stream
@@ -199,7 +216,8 @@ const char* ar_last_error(const ar_ctx* ctx);
 
 /* Name of the kernel variant the last successful call launched (tests assert on it):
  * "reduce_vec", "reduce_vec_tail", "reduce_scalar", "fused_row_vec", "fused_cluster_vec",
- * "fused_staged", "fused_scalar", "fused_cluster_scalar" or "none" (empty call). */
+ * "fused_staged", "fused_scalar", "fused_cluster_scalar", "fused_batch",
+ * "fused_batch_sequential" or "none" (empty call). */
 const char* ar_last_variant(const ar_ctx* ctx);
 
 /* Tuning and test overrides (0 = automatic for each, except AR_OPT_PDL).  Values outside

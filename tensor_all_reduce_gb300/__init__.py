@@ -29,6 +29,7 @@ AR_DTYPE_F32 = 0
 AR_DTYPE_F16 = 1
 AR_DTYPE_BF16 = 2
 AR_MAX_PARTIALS = 8
+AR_MAX_BATCH = 16
 AR_QUANT_NONE = 0
 AR_QUANT_FP8_E4M3_PER_TOKEN = 1
 
@@ -101,8 +102,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ar_set_option.argtypes = [vp, c_int, i64]
     lib.ar_get_info.argtypes = [vp, c_int, ctypes.POINTER(i64)]
     lib.ar_device_status.argtypes = [vp, ctypes.POINTER(c_int)]
+    lib.ar_fused_reduce_rmsnorm_batch.argtypes = [vp, ctypes.POINTER(ArFusedArgs), c_int, vp]
     for f in ("ar_init", "ar_destroy", "ar_reduce_sum", "ar_fused_reduce_rmsnorm", "ar_set_option",
-              "ar_get_info", "ar_device_status"):
+              "ar_get_info", "ar_device_status", "ar_fused_reduce_rmsnorm_batch"):
         getattr(lib, f).restype = c_int
     _lib = lib
     return lib
@@ -182,6 +184,15 @@ def ar_fused_reduce_rmsnorm(ctx: int, args: ArFusedArgs, stream: Optional[int] =
     st = load_library().ar_fused_reduce_rmsnorm(ctx, ctypes.byref(args), stream)
     if raise_on_error:
         _check(ctx, st, "ar_fused_reduce_rmsnorm")
+    return st
+
+
+def ar_fused_reduce_rmsnorm_batch(ctx: int, calls: Sequence[ArFusedArgs], stream: Optional[int] = None,
+                                  raise_on_error: bool = True) -> int:
+    arr = (ArFusedArgs * max(len(calls), 1))(*calls)
+    st = load_library().ar_fused_reduce_rmsnorm_batch(ctx, arr, len(calls), stream)
+    if raise_on_error:
+        _check(ctx, st, "ar_fused_reduce_rmsnorm_batch")
     return st
 
 
@@ -304,3 +315,33 @@ class Context:
                                m, h, _torch_dtype_code(x0), skip_norm=skip_norm, out_fp32=out_fp32)
         ar_fused_reduce_rmsnorm(self.handle, args, _stream(stream))
         return out, residual_out, q_out, scale_out
+
+    def fused_reduce_rmsnorm_batch(self, calls, stream=None):
+        """Several independent fused calls in one launch.  `calls` is a list of dicts with the
+        keyword arguments of fused_reduce_rmsnorm (partials, residual, weight, eps, gemma,
+        quant, out, residual_out, q_out, scale_out, skip_norm, out_fp32); missing outputs are
+        allocated.  Returns a list of (out, residual_out, q_out, scale_out)."""
+        import torch
+        results, args = [], []
+        for c in calls:
+            x0 = c["partials"][0]
+            m, h = x0.shape
+            quant, out_fp32 = c.get("quant", False), c.get("out_fp32", False)
+            out = c.get("out")
+            if out is None and (c.get("want_out", True) or not quant):
+                out = torch.empty((m, h), dtype=torch.float32 if out_fp32 else x0.dtype, device=x0.device)
+            ro = c.get("residual_out")
+            if ro is None and c.get("want_residual_out", True):
+                ro = torch.empty_like(x0)
+            q = c.get("q_out")
+            sc = c.get("scale_out")
+            if quant:
+                q = q if q is not None else torch.empty((m, h), dtype=torch.uint8, device=x0.device)
+                sc = sc if sc is not None else torch.empty((m,), dtype=torch.float32, device=x0.device)
+            args.append(make_fused_args([p.data_ptr() for p in c["partials"]], _ptr(c.get("residual")), _ptr(ro),
+                                        _ptr(c.get("weight")), _ptr(out), c.get("eps", 1e-6), c.get("gemma", False),
+                                        quant, _ptr(q), _ptr(sc), m, h, _torch_dtype_code(x0),
+                                        skip_norm=c.get("skip_norm", False), out_fp32=out_fp32))
+            results.append((out, ro, q, sc))
+        ar_fused_reduce_rmsnorm_batch(self.handle, args, _stream(stream))
+        return results

@@ -120,6 +120,12 @@ int staged_kernel_list(const void** out, int cap) {
           const void* fn = dt ? staged_kernel_bf16(n, ppt, q != 0) : staged_kernel_f16(n, ppt, q != 0);
           if (fn && k < cap) out[k++] = fn;
         }
+  for (int dt = 0; dt < 2; ++dt)
+    for (int n = 1; n <= AR_MAX_PARTIALS; ++n)
+      for (int q = 0; q < 2; ++q) {
+        const void* fn = dt ? batch_kernel_bf16(n, q != 0) : batch_kernel_f16(n, q != 0);
+        if (fn && k < cap) out[k++] = fn;
+      }
   return k;
 }
 }  // namespace ar
@@ -565,6 +571,139 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
     else
       ctx->last_variant = csize > 1 ? "fused_cluster_scalar" : "fused_scalar";
   }
+  return st;
+}
+
+// ---------------------------------------------------------------------------
+// batched fused calls
+// ---------------------------------------------------------------------------
+
+namespace {
+
+struct CallRanges {
+  int nin = 0, nout = 0;
+  const void* in[AR_MAX_PARTIALS + 2];
+  int64_t in_n[AR_MAX_PARTIALS + 2];
+  const void* out[4];
+  int64_t out_n[4];
+};
+
+CallRanges ranges_of(const ar_fused_args* a) {
+  CallRanges r;
+  const int64_t es = elem_size(a->dtype), mh = a->m * a->h, tb = mh * es;
+  for (int k = 0; k < a->n; ++k) { r.in[r.nin] = a->partials[k]; r.in_n[r.nin++] = tb; }
+  if (a->residual_in) { r.in[r.nin] = a->residual_in; r.in_n[r.nin++] = tb; }
+  if (a->weight && !a->skip_norm) { r.in[r.nin] = a->weight; r.in_n[r.nin++] = a->h * es; }
+  if (a->residual_out) { r.out[r.nout] = a->residual_out; r.out_n[r.nout++] = tb; }
+  if (a->out) { r.out[r.nout] = a->out; r.out_n[r.nout++] = mh * (a->out_fp32 ? 4 : es); }
+  if (a->quant) {
+    r.out[r.nout] = a->q_out; r.out_n[r.nout++] = mh;
+    r.out[r.nout] = a->scale_out; r.out_n[r.nout++] = a->m * 4;
+  }
+  return r;
+}
+
+}  // namespace
+
+extern "C" ar_status ar_fused_reduce_rmsnorm_batch(ar_ctx* ctx, const ar_fused_args* calls, int count,
+                                                   void* stream) {
+  if (!calls || count < 1 || count > AR_MAX_BATCH) return AR_ERR_INVALID_ARG;
+  for (int i = 0; i < count; ++i) {  // each call by the single-call rules (checked before any context use)
+    const ar_status v = ar_fused_reduce_rmsnorm(nullptr, &calls[i], stream);
+    if (v != AR_ERR_NOT_INITIALIZED) return v;
+  }
+  const ar_fused_args& c0 = calls[0];
+  for (int i = 1; i < count; ++i) {
+    const ar_fused_args& c = calls[i];
+    if (c.n != c0.n || c.dtype != c0.dtype || c.quant != c0.quant || (c.skip_norm != 0) != (c0.skip_norm != 0) ||
+        (c.out_fp32 != 0) != (c0.out_fp32 != 0))
+      return AR_ERR_INVALID_ARG;
+  }
+  // the calls run at the same time: no call may write what another call reads or writes
+  CallRanges rg[AR_MAX_BATCH];
+  for (int i = 0; i < count; ++i) rg[i] = ranges_of(&calls[i]);
+  for (int i = 0; i < count; ++i)
+    for (int j = 0; j < count; ++j) {
+      if (i == j) continue;
+      for (int o = 0; o < rg[i].nout; ++o) {
+        for (int k = 0; k < rg[j].nin; ++k)
+          if (overlaps(rg[i].out[o], rg[i].out_n[o], rg[j].in[k], rg[j].in_n[k])) return AR_ERR_OVERLAP;
+        for (int k = 0; k < rg[j].nout; ++k)
+          if (overlaps(rg[i].out[o], rg[i].out_n[o], rg[j].out[k], rg[j].out_n[k])) return AR_ERR_OVERLAP;
+      }
+    }
+  if (!ctx) return AR_ERR_NOT_INITIALIZED;
+
+  // one launch when every call can take the staged path with one stage per CTA
+  bool one = true;
+  int64_t total_rows = 0, max_stage = 0;
+  int max_row_packs = 1;
+  for (int i = 0; i < count; ++i) {
+    const ar_fused_args& a = calls[i];
+    bool vec = (a.h % 8) == 0 && a.h <= 8192;
+    for (int r = 0; r < a.n; ++r) vec = vec && aligned(a.partials[r], 16);
+    vec = vec && aligned(a.residual_in, 16) && aligned(a.residual_out, 16) && aligned(a.weight, 16) &&
+          aligned(a.out, 16) && (!a.quant || aligned(a.q_out, 8));
+    one = one && vec;
+    total_rows += a.m;
+    const int64_t stage = (int64_t)(a.n + (a.residual_in ? 1 : 0)) * a.h * elem_size(a.dtype);
+    if (stage > max_stage) max_stage = stage;
+    if ((int)(a.h / 8) > max_row_packs) max_row_packs = (int)(a.h / 8);
+  }
+  one = one && max_stage <= ctx->max_dyn_smem && total_rows <= 0x7FFFFFFFLL;
+  if (total_rows == 0) {
+    ctx->last_variant = "none";
+    return AR_OK;
+  }
+  if (!one) {
+    for (int i = 0; i < count; ++i) {
+      const ar_status st = ar_fused_reduce_rmsnorm(ctx, &calls[i], stream);
+      if (st != AR_OK) return st;
+    }
+    ctx->last_variant = "fused_batch_sequential";
+    return AR_OK;
+  }
+
+  ar::BatchParams bp;
+  memset(&bp, 0, sizeof(bp));
+  bp.count = count;
+  bp.sp.stages = 1;
+  bp.sp.err = ctx->d_status;
+  bp.sp.wait_cycles = 2000000000LL;
+  int64_t acc = 0;
+  for (int i = 0; i < count; ++i) {
+    const ar_fused_args& a = calls[i];
+    ar::FusedParams& p = bp.call[i];
+    for (int r = 0; r < a.n; ++r) p.x[r] = a.partials[r];
+    p.res_in = a.residual_in;
+    p.res_out = a.residual_out;
+    p.w = a.weight;
+    p.out = a.out;
+    p.q = static_cast<uint8_t*>(a.q_out);
+    p.scale = a.scale_out;
+    p.m = a.m;
+    p.h = (int)a.h;
+    p.row_packs = (int)(a.h / 8);
+    p.chunk_packs = p.row_packs;
+    p.csize = 1;
+    p.eps = a.eps;
+    p.inv_h = (float)(1.0 / (double)a.h);
+    p.gemma = a.gemma != 0;
+    p.skip_norm = a.skip_norm != 0;
+    p.out_f32 = a.out_fp32 != 0 && a.out != nullptr;
+    bp.row_start[i] = acc;
+    acc += a.m;
+  }
+  bp.row_start[count] = acc;
+  const bool quant = c0.quant == AR_QUANT_FP8_E4M3_PER_TOKEN;
+  const void* fn = c0.dtype == AR_DTYPE_BF16 ? ar::batch_kernel_bf16(c0.n, quant) : ar::batch_kernel_f16(c0.n, quant);
+  if (!fn) return AR_ERR_UNSUPPORTED;
+  int block = ((max_row_packs + 1) / 2 + 31) / 32 * 32;
+  if (block < 32) block = 32;
+  DeviceGuard g(ctx->device);
+  void* args[1] = {&bp};
+  const ar_status st = launch(ctx, fn, (unsigned)total_rows, (unsigned)block, 1, args, (size_t)max_stage, stream);
+  if (st == AR_OK) ctx->last_variant = "fused_batch";
   return st;
 }
 

@@ -18,6 +18,10 @@ const void* fused_kernel_bf16(int n, int ppt, bool quant, bool vec);
 const void* staged_kernel_f16(int n, int ppt, bool quant);
 const void* staged_kernel_bf16(int n, int ppt, bool quant);
 
+// Batched form of the staged kernel (2 packs per thread, one row per CTA).
+const void* batch_kernel_f16(int n, bool quant);
+const void* batch_kernel_bf16(int n, bool quant);
+
 // Every fused kernel entry, for one-time attribute setup (non-portable cluster sizes).
 int fused_kernel_list(const void** out, int cap);
 int staged_kernel_list(const void** out, int cap);

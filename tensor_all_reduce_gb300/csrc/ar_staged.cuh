@@ -92,8 +92,11 @@ __device__ __forceinline__ uint4 lds_v4(const void* p) {
   return v;
 }
 
+// The rows r = first + i * stride (i = 0, 1, ...) of one call, processed by this CTA
+// through its shared-memory ring.  Shared by the persistent kernel and the batched one.
 template <int DT, int N, int PPT, bool QUANT>
-__global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedParams p, const StagedParams sp) {
+__device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedParams& sp, int64_t first,
+                                            int64_t stride) {
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ __align__(8) uint64_t full_bar[4];
   __shared__ float red_ss[2][32];
@@ -104,7 +107,6 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
   const int rows_per_stage = N + (has_res ? 1 : 0);
   const uint32_t row_bytes = (uint32_t)sp.row_bytes;
   const uint32_t stage_bytes = row_bytes * (uint32_t)rows_per_stage;
-  const int64_t first = blockIdx.x, stride = gridDim.x;
   const int64_t my_rows = first < p.m ? (p.m - first + stride - 1) / stride : 0;
 
   if (threadIdx.x == 0) {
@@ -262,6 +264,35 @@ __global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedPar
       }
     }
   }
+}
+
+template <int DT, int N, int PPT, bool QUANT>
+__global__ void __launch_bounds__(1024 / PPT) fused_staged_kernel(const FusedParams p, const StagedParams sp) {
+  staged_rows<DT, N, PPT, QUANT>(p, sp, blockIdx.x, gridDim.x);
+}
+
+// ---------------------------------------------------------------------------
+// Batched form: up to kMaxBatch independent calls (same N, element type and options) in
+// one launch.  CTA b serves row b - row_start[c] of the call c with
+// row_start[c] <= b < row_start[c + 1], one row per CTA, with one shared-memory stage.
+// ---------------------------------------------------------------------------
+constexpr int kMaxBatch = 16;
+
+struct BatchParams {
+  int count;
+  int64_t row_start[kMaxBatch + 1];
+  StagedParams sp;  // row_bytes is per call: taken from call[c].h
+  FusedParams call[kMaxBatch];
+};
+
+template <int DT, int N, int PPT, bool QUANT>
+__global__ void __launch_bounds__(1024 / PPT) fused_batch_kernel(const BatchParams bp) {
+  int c = 0;
+  while (c + 1 < bp.count && (int64_t)blockIdx.x >= bp.row_start[c + 1]) ++c;
+  const int64_t row = (int64_t)blockIdx.x - bp.row_start[c];
+  StagedParams sp = bp.sp;
+  sp.row_bytes = bp.call[c].h * 2;
+  staged_rows<DT, N, PPT, QUANT>(bp.call[c], sp, row, bp.call[c].m);
 }
 
 }  // namespace ar

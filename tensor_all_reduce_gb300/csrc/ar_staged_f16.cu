@@ -24,4 +24,14 @@ const void* staged_kernel_f16(int n, int ppt, bool quant) {
   }
 }
 
+const void* batch_kernel_f16(int n, bool quant) {
+  switch (n) {
+#define AR_CASE(NN) \
+  case NN: return quant ? (const void*)&fused_batch_kernel<kF16, NN, 2, true> : (const void*)&fused_batch_kernel<kF16, NN, 2, false>;
+    AR_CASE(1) AR_CASE(2) AR_CASE(3) AR_CASE(4) AR_CASE(5) AR_CASE(6) AR_CASE(7) AR_CASE(8)
+#undef AR_CASE
+    default: return nullptr;
+  }
+}
+
 }  // namespace ar

@@ -144,3 +144,26 @@ def test_fused_validation(lib):
 def test_options_reject_out_of_range_values(lib):
     # ar_set_option checks the context first; the value ranges are exercised on the GPU
     assert lib.ar_set_option(None, 99, 0) == tar.AR_ERR_NOT_INITIALIZED
+
+
+def test_batch_validation(lib):
+    def call(base, **kw):
+        d = dict(partials=[base + i * 64 * MB for i in range(4)], residual_in=base + 4 * 64 * MB,
+                 residual_out=base + 5 * 64 * MB, weight=BASE + 6 * 64 * MB, out=base + 7 * 64 * MB,
+                 eps=1e-6, gemma=False, quant=False, q_out=None, scale_out=None, m=16, h=6144,
+                 dtype=tar.AR_DTYPE_BF16)
+        d.update(kw)
+        return tar.make_fused_args(**d)
+
+    B2 = BASE + (1 << 36)
+    NI, IA, OV = tar.AR_ERR_NOT_INITIALIZED, tar.AR_ERR_INVALID_ARG, tar.AR_ERR_OVERLAP
+    st = lambda calls: tar.ar_fused_reduce_rmsnorm_batch(None, calls, None, raise_on_error=False)
+    assert st([call(BASE), call(B2)]) == NI                         # shared weight is fine
+    assert st([]) == IA
+    assert st([call(BASE + i * (1 << 33)) for i in range(tar.AR_MAX_BATCH + 1)]) == IA
+    assert st([call(BASE), call(B2, partials=[B2, B2 + 64 * MB])]) == IA       # different n
+    assert st([call(BASE), call(B2, dtype=tar.AR_DTYPE_F16)]) == IA
+    assert st([call(BASE), call(B2, out=BASE)]) == OV               # writes call 0's partial
+    assert st([call(BASE), call(B2, residual_out=BASE + 5 * 64 * MB)]) == OV   # same output
+    assert st([call(BASE), call(B2, h=0)]) == IA                    # per-call rules apply
+
