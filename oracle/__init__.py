@@ -68,7 +68,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
                                              c_float, c_int, c_int, c_int]
     lib.orc_fused_reduce_rmsnorm.restype = c_int
     lib.orc_fused_ex.argtypes = [vp, vp, vp, vp, vp, vp, c_int, vp, vp, i64, i64, c_float, c_int, c_int,
-                                 c_int, c_int]
+                                 c_int, i64, c_int]
+    lib.orc_per_group_quant.argtypes = [vp, vp, vp, i64, i64, i64, c_int]
+    lib.orc_per_group_quant.restype = c_int
     lib.orc_fused_ex.restype = c_int
     return lib
 
@@ -185,23 +187,35 @@ class Oracle:
             raise ValueError(f"orc_fused_reduce_rmsnorm rejected its arguments ({rc})")
         return {"y": y, "res_out": res_out, "q": q, "scale": scale}
 
+    def per_group_quant(self, y, group: int, dtype: str):
+        """dynamic per-group FP8 e4m3 quantisation: returns (q [m, h], scale [m, h // group])."""
+        y = np.ascontiguousarray(y)
+        m, h = y.shape
+        q = np.empty((m, h), np.uint8)
+        scale = np.empty((m, h // group), np.float32)
+        rc = self.lib.orc_per_group_quant(self._ptr(q), self._ptr(scale), self._ptr(y), m, h, group, DTYPES[dtype])
+        if rc != 0:
+            raise ValueError(f"orc_per_group_quant rejected its arguments ({rc})")
+        return q, scale
+
     def fused_ex(self, partials: Sequence[np.ndarray], res_in, w, eps: float, gemma: bool, quant: bool,
-                 dtype: str, skip_norm: bool = False, out_fp32: bool = False) -> dict:
-        """The whole path with the skip-norm and fp32-output options.  Returns y (16-bit bits),
-        y32 (float32, when out_fp32), res_out, q, scale."""
+                 dtype: str, skip_norm: bool = False, out_fp32: bool = False, group: int = 0) -> dict:
+        """The whole path with the skip-norm, fp32-output and per-group-FP8 options.  Returns y
+        (16-bit bits), y32 (float32, when out_fp32), res_out, q, scale ([m] per token, or
+        [m, h // group] per group)."""
         ps = [np.ascontiguousarray(p) for p in partials]
         m, h = ps[0].shape
         y = np.empty((m, h), np.uint16)
         y32 = np.empty((m, h), np.float32) if out_fp32 else None
         res_out = np.empty((m, h), np.uint16)
         q = np.empty((m, h), np.uint8) if quant else None
-        scale = np.empty((m,), np.float32) if quant else None
+        scale = (np.empty((m, h // group) if group else (m,), np.float32)) if quant else None
         arr = (ctypes.c_void_p * len(ps))(*[self._ptr(p) for p in ps])
         rc = self.lib.orc_fused_ex(
             self._ptr(y), self._ptr(y32), self._ptr(res_out), self._ptr(q), self._ptr(scale), arr, len(ps),
             self._ptr(None if res_in is None else np.ascontiguousarray(res_in)),
             self._ptr(None if w is None else np.ascontiguousarray(w)), m, h, eps, int(bool(gemma)),
-            int(bool(quant)), int(bool(skip_norm)), DTYPES[dtype])
+            int(bool(quant)), int(bool(skip_norm)), int(group), DTYPES[dtype])
         if rc != 0:
             raise ValueError(f"orc_fused_ex rejected its arguments ({rc})")
         return {"y": y, "y32": y32, "res_out": res_out, "q": q, "scale": scale}

@@ -297,6 +297,31 @@ int orc_per_token_quant(uint8_t* q, float* scale, const void* y, int64_t m, int6
   return 0;
 }
 
+/* Dynamic per-group quantisation of one rounded row of h elements: every run of g
+ * consecutive elements (h a multiple of g) gets its own scale amax_group / 448 and its
+ * codes, with the per-token rules inside the group. */
+static void quant_row_groups(uint8_t* q, float* scale, const void* y, int64_t h, int64_t g, int dtype) {
+  for (int64_t k = 0; k < h / g; ++k) {
+    const int64_t j0 = k * g, j1 = j0 + g;
+    float amax = 0.0f;
+    for (int64_t j = j0; j < j1; ++j) {
+      float a = fabsf(load_elem(y, j, dtype));
+      if (a > amax) amax = a;
+    }
+    float sc = amax / 448.0f;
+    scale[k] = sc;
+    for (int64_t j = j0; j < j1; ++j) q[j] = amax == 0.0f ? 0 : orc_f32_to_e4m3(load_elem(y, j, dtype) / sc);
+  }
+}
+
+int orc_per_group_quant(uint8_t* q, float* scale, const void* y, int64_t m, int64_t h, int64_t group, int dtype) {
+  if (!q || !scale || !y || m < 0 || h < 1 || group < 1 || h % group != 0) return -1;
+  if (dtype != ORC_F16 && dtype != ORC_BF16) return -1;
+  for (int64_t r = 0; r < m; ++r)
+    quant_row_groups(q + r * h, scale + r * (h / group), (const uint16_t*)y + r * h, h, group, dtype);
+  return 0;
+}
+
 /* ---------------------------------------------------------------------- */
 /* the composition                                                         */
 /* ---------------------------------------------------------------------- */
@@ -304,13 +329,14 @@ int orc_per_token_quant(uint8_t* q, float* scale, const void* y, int64_t m, int6
 int orc_fused_reduce_rmsnorm(void* y, void* res_out, uint8_t* q, float* scale,
                              const void* const* partials, int n, const void* res_in, const void* w,
                              int64_t m, int64_t h, float eps, int gemma, int quant, int dtype) {
-  return orc_fused_ex(y, NULL, res_out, q, scale, partials, n, res_in, w, m, h, eps, gemma, quant, 0, dtype);
+  return orc_fused_ex(y, NULL, res_out, q, scale, partials, n, res_in, w, m, h, eps, gemma, quant, 0, 0, dtype);
 }
 
 int orc_fused_ex(void* y, float* y32, void* res_out, uint8_t* q, float* scale, const void* const* partials,
                  int n, const void* res_in, const void* w, int64_t m, int64_t h, float eps, int gemma,
-                 int quant, int skip_norm, int dtype) {
+                 int quant, int skip_norm, int64_t group, int dtype) {
   if (!partials || n < 1 || (!w && !skip_norm) || m < 0 || h < 1) return -1;
+  if (group < 0 || (group > 0 && h % group != 0)) return -1;
   if (dtype != ORC_F16 && dtype != ORC_BF16) return -1;
   if (quant && (!q || !scale)) return -1;
   if (!quant && !y && !y32) return -1;
@@ -336,7 +362,8 @@ int orc_fused_ex(void* y, float* y32, void* res_out, uint8_t* q, float* scale, c
                        skip_norm, dtype);
     if (res_out) memcpy((uint16_t*)res_out + base, ro_row, row_bytes);
     if (y) memcpy((uint16_t*)y + base, y_row, row_bytes);
-    if (quant) quant_row(q + base, scale + r, y_row, 0, h, dtype);
+    if (quant && group) quant_row_groups(q + base, scale + r * (h / group), y_row, h, group, dtype);
+    else if (quant) quant_row(q + base, scale + r, y_row, 0, h, dtype);
   }
   free(s_row); free(z_row); free(y_row); free(ro_row); free(row_ptrs);
   return 0;

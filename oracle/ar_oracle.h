@@ -85,15 +85,21 @@ int orc_fused_reduce_rmsnorm(void* y, void* res_out, uint8_t* q, float* scale,
                              const void* const* partials, int n, const void* res_in, const void* w,
                              int64_t m, int64_t h, float eps, int gemma, int quant, int dtype);
 
+/* dynamic per-group quantisation of rounded rows y [m, h] in groups of `group`
+ * consecutive elements (h a multiple of group): scale [m, h / group], each group with the
+ * per-token rules (amax / 448, binary32 quotient, zero group -> scale 0, codes 0). */
+int orc_per_group_quant(uint8_t* q, float* scale, const void* y, int64_t m, int64_t h, int64_t group, int dtype);
+
 /* The whole path with its two options.
  *   y32 (may be NULL): the normalised row as binary32, RN_f32 of the binary64 value
  *       z * inv * w' (no rounding to the 16-bit type first);
  *   skip_norm: no normalisation, the output is z itself (the rounded sum plus residual);
  *       w may then be NULL and eps, gemma are unused.
- * The FP8 epilogue always quantises the 16-bit output (z with skip_norm). */
+ * The FP8 epilogue always quantises the 16-bit output (z with skip_norm); group > 0 makes
+ * it per-group (scale [m, h / group]) instead of per-token (scale [m]). */
 int orc_fused_ex(void* y, float* y32, void* res_out, uint8_t* q, float* scale, const void* const* partials,
                  int n, const void* res_in, const void* w, int64_t m, int64_t h, float eps, int gemma,
-                 int quant, int skip_norm, int dtype);
+                 int quant, int skip_norm, int64_t group, int dtype);
 
 #ifdef __cplusplus
 }

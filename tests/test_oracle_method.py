@@ -354,3 +354,49 @@ def test_fp32_output_closed_forms(orc):
     assert list(out["y32"][0]) == [1.0] * 4
     assert list(out["y32"][1]) == [2.0, 0.0, 0.0, 0.0]
 
+
+# ---------------------------------------------------------------------------
+# per-group FP8 (groups of G consecutive elements along a row)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("group", [8, 32, 128])
+def test_per_group_quant_is_per_token_quant_of_the_groups(orc, dtype, group):
+    """Cutting every row into groups and quantising each group as its own token gives the
+    per-group result: the per-token routine (pinned above) run on the [m * h / G, G] view."""
+    inp = synth.fused_inputs(1, 6, 512, dtype, seed=41)
+    y = synth.bits(inp["partials"][0])
+    y[2, 64:192] = 0                                   # zero groups
+    q, sc = orc.per_group_quant(y, group, dtype)
+    q2, sc2 = orc.per_token_quant(y.reshape(-1, group), dtype)
+    assert np.array_equal(q, q2.reshape(q.shape))
+    assert np.array_equal(sc, sc2.reshape(sc.shape))
+    # one group per row is per-token quantisation
+    q3, sc3 = orc.per_group_quant(y, 512, dtype)
+    q4, sc4 = orc.per_token_quant(y, dtype)
+    assert np.array_equal(q3, q4) and np.array_equal(sc3.ravel(), sc4)
+
+
+def test_per_group_scales_follow_their_own_groups(orc):
+    # row 0: groups of 4 with maxima 1, 2, 4, 8 -> scales max/448, and each group's max -> 448
+    vals = np.array([[0.5, 1.0, -0.25, 0.75, 2.0, -1.0, 0.0, 1.5, 4.0, 3.0, -2.0, 1.0, -8.0, 0.5, 4.0, 2.0]],
+                    np.float32)
+    y = _t(vals.tolist(), "bf16")
+    q, sc = orc.per_group_quant(y, 4, "bf16")
+    assert list(sc[0]) == [np.float32(x) / np.float32(448) for x in (1.0, 2.0, 4.0, 8.0)]
+    assert q[0, 1] == 0x7E and q[0, 4] == 0x7E and q[0, 8] == 0x7E and q[0, 12] == 0xFE
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_fused_with_per_group_quant(orc, dtype):
+    inp = synth.fused_inputs(4, 5, 384, dtype, seed=43, gemma=True)
+    ps = [synth.bits(p) for p in inp["partials"]]
+    res, w = synth.bits(inp["residual"]), synth.bits(inp["weight"])
+    out = orc.fused_ex(ps, res, w, 1e-6, True, True, dtype, group=64)
+    q, sc = orc.per_group_quant(out["y"], 64, dtype)
+    assert np.array_equal(out["q"], q) and np.array_equal(out["scale"], sc)
+    assert out["scale"].shape == (5, 6)
+    # the rest of the path is unchanged by the grouping
+    ref = orc.fused(ps, res, w, 1e-6, True, True, dtype)
+    assert np.array_equal(out["y"], ref["y"]) and np.array_equal(out["res_out"], ref["res_out"])
+

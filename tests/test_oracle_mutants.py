@@ -33,7 +33,7 @@ MUTANTS = [
     ("norm_reads_sum_not_residual_sum",
      "double zv = (double)load_elem(z_row, j, dtype);\n    double wv",
      "double zv = (double)load_elem(s, base + j, dtype);\n    double wv"),
-    ("fp8_max_240", "float sc = amax / 448.0f;", "float sc = amax / 240.0f;"),
+    ("fp8_max_240", "  float sc = amax / 448.0f;\n  scale[row] = sc;", "  float sc = amax / 240.0f;\n  scale[row] = sc;"),
     ("scale_row_index", "scale[row] = sc;", "scale[0] = sc;"),
     ("quant_of_unrounded_z", "if (quant) quant_row(q + base, scale + r, y_row, 0, h, dtype);",
      "if (quant) quant_row(q + base, scale + r, z_row, 0, h, dtype);"),
@@ -52,6 +52,9 @@ MUTANTS = [
     ("skip_norm_outputs_the_sum", "if (y32) y32[base + j] = load_elem(z_row, j, dtype);",
      "if (y32) y32[base + j] = load_elem(s, base + j, dtype);"),
     ("skip_norm_still_normalises", "  if (skip_norm) {\n", "  if (0) {\n"),
+    ("group_bounds_off_by_one", "const int64_t j0 = k * g, j1 = j0 + g;", "const int64_t j0 = k * g, j1 = j0 + g - 1;"),
+    ("group_scale_index", "scale + r * (h / group), (const uint16_t*)y + r * h", "scale + r, (const uint16_t*)y + r * h"),
+    ("group_max_448_240", "    float sc = amax / 448.0f;\n    scale[k] = sc;", "    float sc = amax / 240.0f;\n    scale[k] = sc;"),
 ]
 
 
