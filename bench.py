@@ -188,7 +188,8 @@ class FusedSets:
         self.out = torch.empty((sets, m, h), dtype=torch.float32 if wl.out_fp32 else t, device=dev) if want_y else None
         self.ro = torch.empty((sets, m, h), dtype=t, device=dev) if wl.residual else None
         self.q = torch.empty((sets, m, h), dtype=torch.uint8, device=dev) if wl.quant else None
-        self.sc = torch.empty((sets, m), dtype=torch.float32, device=dev) if wl.quant else None
+        ns = m * (h // wl.group) if wl.group else m
+        self.sc = torch.empty((sets, ns), dtype=torch.float32, device=dev) if wl.quant else None
         for k in range(n):
             self.parts[:, k].copy_(inp["partials"][k].to(dev).unsqueeze(0).expand(sets, m, h))
         if self.res is not None:
@@ -204,7 +205,7 @@ class FusedSets:
                                  q_out=None if self.q is None else self.q[r],
                                  scale_out=None if self.sc is None else self.sc[r],
                                  want_out=self.out is not None, want_residual_out=self.ro is not None,
-                                 skip_norm=wl.skip_norm, out_fp32=wl.out_fp32)
+                                 skip_norm=wl.skip_norm, out_fp32=wl.out_fp32, group_size=wl.group)
 
 
 class BatchSets:

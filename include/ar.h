@@ -65,7 +65,11 @@ typedef enum { AR_DTYPE_F32 = 0, AR_DTYPE_F16 = 1, AR_DTYPE_BF16 = 2 } ar_dtype;
  * Results; [P1] Test results runs TP2/TP4). */
 #define AR_MAX_PARTIALS 8
 
-enum { AR_QUANT_NONE = 0, AR_QUANT_FP8_E4M3_PER_TOKEN = 1 };
+/* FP8 epilogue modes.  PER_GROUP (SURVEY-ranked follow-up of the per-group form [P1]
+ * names without a group size or scale rule): every run of group_size consecutive elements
+ * of a row gets its own scale amax_group / 448 and codes by the per-token rules; scales
+ * are [m, h / group_size] fp32 row-major. */
+enum { AR_QUANT_NONE = 0, AR_QUANT_FP8_E4M3_PER_TOKEN = 1, AR_QUANT_FP8_E4M3_PER_GROUP = 2 };
 
 /*
  * Create a context for CUDA device `device` (flags: must be 0).  Queries the SM count,
@@ -119,9 +123,10 @@ typedef struct {
                                               NULL allowed only when quant is on */
   float eps;                               /* finite, >= 0 */
   int gemma;                               /* != 0: weight factor is (1 + w) ([P1] gemma_norm) */
-  int quant;                               /* AR_QUANT_NONE or AR_QUANT_FP8_E4M3_PER_TOKEN */
+  int quant;                               /* AR_QUANT_NONE, _FP8_E4M3_PER_TOKEN or _FP8_E4M3_PER_GROUP */
   void* q_out;                             /* device [m, h] E4M3 bytes, required when quant is on */
-  float* scale_out;                        /* device [m] fp32 per-row scales, required when quant is on */
+  float* scale_out;                        /* device fp32 scales, required when quant is on: [m] per
+                                              token, [m, h / group_size] per group */
   int64_t m;                               /* rows (tokens), >= 0 (0 launches nothing; then
                                               only weight must be non-NULL) */
   int64_t h;                               /* hidden size, >= 1 */
@@ -133,6 +138,8 @@ typedef struct {
   int out_fp32;                            /* != 0: `out` is [m, h] fp32 and receives the normalised
                                               row before its rounding to dtype (the FP8 epilogue still
                                               quantises the dtype-rounded row) */
+  int group_size;                          /* per-group FP8: 8, 16, 32, 64, 128 or 256 elements,
+                                              dividing h, with h <= 8192; ignored otherwise */
 } ar_fused_args;
 
 /*

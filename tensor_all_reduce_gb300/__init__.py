@@ -32,6 +32,7 @@ AR_MAX_PARTIALS = 8
 AR_MAX_BATCH = 16
 AR_QUANT_NONE = 0
 AR_QUANT_FP8_E4M3_PER_TOKEN = 1
+AR_QUANT_FP8_E4M3_PER_GROUP = 2
 
 AR_OPT_FORCE_VARIANT = 0
 AR_OPT_CLUSTER_SIZE = 1
@@ -65,6 +66,7 @@ class ArFusedArgs(ctypes.Structure):
         ("dtype", ctypes.c_int),
         ("skip_norm", ctypes.c_int),
         ("out_fp32", ctypes.c_int),
+        ("group_size", ctypes.c_int),
     ]
 
 
@@ -199,7 +201,7 @@ def ar_fused_reduce_rmsnorm_batch(ctx: int, calls: Sequence[ArFusedArgs], stream
 def make_fused_args(partials: Sequence[int], residual_in: Optional[int], residual_out: Optional[int],
                     weight: Optional[int], out: Optional[int], eps: float, gemma: bool, quant: bool,
                     q_out: Optional[int], scale_out: Optional[int], m: int, h: int, dtype: int,
-                    skip_norm: bool = False, out_fp32: bool = False) -> ArFusedArgs:
+                    skip_norm: bool = False, out_fp32: bool = False, group_size: int = 0) -> ArFusedArgs:
     a = ArFusedArgs()
     a.n = len(partials)
     for i, p in enumerate(partials):
@@ -210,7 +212,8 @@ def make_fused_args(partials: Sequence[int], residual_in: Optional[int], residua
     a.out = out
     a.eps = eps
     a.gemma = int(bool(gemma))
-    a.quant = AR_QUANT_FP8_E4M3_PER_TOKEN if quant else AR_QUANT_NONE
+    a.quant = (AR_QUANT_FP8_E4M3_PER_GROUP if group_size else AR_QUANT_FP8_E4M3_PER_TOKEN) if quant else AR_QUANT_NONE
+    a.group_size = int(group_size)
     a.q_out = q_out
     a.scale_out = scale_out
     a.m = m
@@ -292,7 +295,7 @@ class Context:
     def fused_reduce_rmsnorm(self, partials, residual, weight, eps: float = 1e-6, gemma: bool = False,
                              quant: bool = False, out=None, residual_out=None, q_out=None, scale_out=None,
                              want_out: bool = True, want_residual_out: bool = True, stream=None,
-                             skip_norm: bool = False, out_fp32: bool = False):
+                             skip_norm: bool = False, out_fp32: bool = False, group_size: int = 0):
         """Returns (out, residual_out, q_out, scale_out); absent outputs are None.  With
         skip_norm there is no RMSNorm (weight may be None); with out_fp32 `out` is float32."""
         import torch
@@ -309,10 +312,12 @@ class Context:
             if q_out is None:
                 q_out = torch.empty((m, h), dtype=torch.uint8, device=x0.device)
             if scale_out is None:
-                scale_out = torch.empty((m,), dtype=torch.float32, device=x0.device)
+                shape = (m, h // group_size) if group_size else (m,)
+                scale_out = torch.empty(shape, dtype=torch.float32, device=x0.device)
         args = make_fused_args([p.data_ptr() for p in partials], _ptr(residual), _ptr(residual_out),
                                _ptr(weight), _ptr(out), eps, gemma, quant, _ptr(q_out), _ptr(scale_out),
-                               m, h, _torch_dtype_code(x0), skip_norm=skip_norm, out_fp32=out_fp32)
+                               m, h, _torch_dtype_code(x0), skip_norm=skip_norm, out_fp32=out_fp32,
+                               group_size=group_size)
         ar_fused_reduce_rmsnorm(self.handle, args, _stream(stream))
         return out, residual_out, q_out, scale_out
 
@@ -335,13 +340,15 @@ class Context:
                 ro = torch.empty_like(x0)
             q = c.get("q_out")
             sc = c.get("scale_out")
+            g = c.get("group_size", 0)
             if quant:
                 q = q if q is not None else torch.empty((m, h), dtype=torch.uint8, device=x0.device)
-                sc = sc if sc is not None else torch.empty((m,), dtype=torch.float32, device=x0.device)
+                sc = sc if sc is not None else torch.empty((m, h // g) if g else (m,), dtype=torch.float32,
+                                                           device=x0.device)
             args.append(make_fused_args([p.data_ptr() for p in c["partials"]], _ptr(c.get("residual")), _ptr(ro),
                                         _ptr(c.get("weight")), _ptr(out), c.get("eps", 1e-6), c.get("gemma", False),
                                         quant, _ptr(q), _ptr(sc), m, h, _torch_dtype_code(x0),
-                                        skip_norm=c.get("skip_norm", False), out_fp32=out_fp32))
+                                        skip_norm=c.get("skip_norm", False), out_fp32=out_fp32, group_size=g))
             results.append((out, ro, q, sc))
         ar_fused_reduce_rmsnorm_batch(self.handle, args, _stream(stream))
         return results

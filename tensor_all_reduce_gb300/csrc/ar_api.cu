@@ -390,8 +390,16 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   if (a->n < 1 || a->n > AR_MAX_PARTIALS || a->m < 0 || a->h < 1 || (!a->weight && !a->skip_norm))
     return AR_ERR_INVALID_ARG;
   if (a->dtype != AR_DTYPE_BF16 && a->dtype != AR_DTYPE_F16) return AR_ERR_INVALID_ARG;
-  if (a->quant != AR_QUANT_NONE && a->quant != AR_QUANT_FP8_E4M3_PER_TOKEN) return AR_ERR_INVALID_ARG;
-  const bool quant = a->quant == AR_QUANT_FP8_E4M3_PER_TOKEN;
+  if (a->quant != AR_QUANT_NONE && a->quant != AR_QUANT_FP8_E4M3_PER_TOKEN && a->quant != AR_QUANT_FP8_E4M3_PER_GROUP)
+    return AR_ERR_INVALID_ARG;
+  const bool quant = a->quant != AR_QUANT_NONE;
+  const bool per_group = a->quant == AR_QUANT_FP8_E4M3_PER_GROUP;
+  if (per_group) {  // groups of 8..256 (a power of two) elements, a whole number per row
+    const int g = a->group_size;
+    if (g < 8 || g > 256 || (g & (g - 1)) != 0 || a->h % g != 0) return AR_ERR_INVALID_ARG;
+    if (a->h > 8192) return AR_ERR_UNSUPPORTED;  // one CTA holds a whole row
+  }
+  const int64_t scale_count = per_group ? a->m * (a->h / a->group_size) : a->m;
   if (!(a->eps >= 0.0f) || isinf(a->eps)) return AR_ERR_INVALID_ARG;  // also rejects NaN
   if (a->h > (int64_t)1 << 30 || a->m > ((int64_t)1 << 40) / a->h) return AR_ERR_INVALID_ARG;
   if (a->m == 0) {  // no rows: only the weight is a real buffer; nothing is touched
@@ -429,7 +437,7 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   if (a->out) outs[no++] = {a->out, mh * oes, !a->out_fp32};
   if (quant) {
     outs[no++] = {a->q_out, mh, false};
-    outs[no++] = {a->scale_out, a->m * 4, false};
+    outs[no++] = {a->scale_out, scale_count * 4, false};
   }
   for (int o = 0; o < no; ++o) {
     for (int i = 0; i < ni; ++i) {
@@ -490,6 +498,8 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
     p.gemma = a->gemma != 0;
     p.skip_norm = a->skip_norm != 0;
     p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
+    p.group_lanes = per_group ? a->group_size / 8 : 0;
+    p.ngroups = per_group ? (int)(a->h / a->group_size) : 0;
     ar::StagedParams sp;
     sp.stages = S;
     sp.row_bytes = (int)(a->h * es);
@@ -525,6 +535,7 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
     while (csize < max_cl && a->m * csize < target && row_packs / (csize * 2) >= 32) csize *= 2;
     if (ctx->force_variant == 2 && csize == 1) csize = 2;
   }
+  if (per_group) csize = 1;  // a group's lanes must sit in one CTA with packs from column 0
   // a CTA holds at most 1024 packs (1024 / ppt threads of ppt packs, the kernels' launch
   // bound): widen the cluster for very long rows
   constexpr int kMaxPacksPerCta = 1024;
@@ -558,6 +569,8 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   p.gemma = a->gemma != 0;
   p.skip_norm = a->skip_norm != 0;
   p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
+  p.group_lanes = per_group ? a->group_size / 8 : 0;
+  p.ngroups = per_group ? (int)(a->h / a->group_size) : 0;
 
   const void* fn = a->dtype == AR_DTYPE_BF16 ? ar::fused_kernel_bf16(a->n, ppt, quant, vec)
                                              : ar::fused_kernel_f16(a->n, ppt, quant, vec);
@@ -597,8 +610,9 @@ CallRanges ranges_of(const ar_fused_args* a) {
   if (a->residual_out) { r.out[r.nout] = a->residual_out; r.out_n[r.nout++] = tb; }
   if (a->out) { r.out[r.nout] = a->out; r.out_n[r.nout++] = mh * (a->out_fp32 ? 4 : es); }
   if (a->quant) {
+    const int64_t ns = a->quant == AR_QUANT_FP8_E4M3_PER_GROUP ? a->m * (a->h / a->group_size) : a->m;
     r.out[r.nout] = a->q_out; r.out_n[r.nout++] = mh;
-    r.out[r.nout] = a->scale_out; r.out_n[r.nout++] = a->m * 4;
+    r.out[r.nout] = a->scale_out; r.out_n[r.nout++] = ns * 4;
   }
   return r;
 }
@@ -691,11 +705,13 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_batch(ar_ctx* ctx, const ar_fused_a
     p.gemma = a.gemma != 0;
     p.skip_norm = a.skip_norm != 0;
     p.out_f32 = a.out_fp32 != 0 && a.out != nullptr;
+    p.group_lanes = a.quant == AR_QUANT_FP8_E4M3_PER_GROUP ? a.group_size / 8 : 0;
+    p.ngroups = a.quant == AR_QUANT_FP8_E4M3_PER_GROUP ? (int)(a.h / a.group_size) : 0;
     bp.row_start[i] = acc;
     acc += a.m;
   }
   bp.row_start[count] = acc;
-  const bool quant = c0.quant == AR_QUANT_FP8_E4M3_PER_TOKEN;
+  const bool quant = c0.quant != AR_QUANT_NONE;
   const void* fn = c0.dtype == AR_DTYPE_BF16 ? ar::batch_kernel_bf16(c0.n, quant) : ar::batch_kernel_f16(c0.n, quant);
   if (!fn) return AR_ERR_UNSUPPORTED;
   int block = ((max_row_packs + 1) / 2 + 31) / 32 * 32;

@@ -44,6 +44,8 @@ struct FusedParams {
   int gemma;
   int skip_norm;     // 1: no normalisation, y = z (weight unused)
   int out_f32;       // 1: `out` holds fp32 values of y before their rounding
+  int group_lanes;   // per-group FP8: lanes (packs) per group, group / 8; 0: per-token FP8
+  int ngroups;       // per-group FP8: groups per row, h / group
 };
 
 // ---------------------------------------------------------------------------
@@ -205,6 +207,28 @@ __device__ __forceinline__ float div_rn_by(float y, float d, float r) {
   const float q0 = y * r;
   const float rem = fmaf(-q0, d, y);
   return copysignf(fmaf(rem, r, q0), y);
+}
+
+// Per-group FP8 of one pack of 8 rounded values y, in groups of `lanes` consecutive packs
+// held by `lanes` consecutive lanes (aligned to `lanes`, which divides 32).  Every lane of
+// the warp must call this (the group's amax is combined with shuffles); the pack's codes
+// are returned, and the first lane of each group stores the group's scale when `store`.
+__device__ __forceinline__ uint2 quant_pack_per_group(const float (&y)[8], int lanes, bool store, float* scale_slot) {
+  float a = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(y[i]));
+  for (int o = 1; o < lanes; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const float scale = __fdiv_rn(a, 448.0f);
+  if (store && (threadIdx.x & (unsigned)(lanes - 1)) == 0) st_f32(scale_slot, scale);
+  const float rcp = a == 0.0f ? 0.0f : __frcp_rn(scale);
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float q0 = a == 0.0f ? 0.0f : div_rn_by(y[2 * i], scale, rcp);
+    const float q1 = a == 0.0f ? 0.0f : div_rn_by(y[2 * i + 1], scale, rcp);
+    c[i] = e4m3x2(q0, q1);
+  }
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
 // ---------------------------------------------------------------------------

@@ -194,7 +194,26 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
   }
 
   // ---- FP8 epilogue ----------------------------------------------------------------
-  if constexpr (QUANT) {
+  if (QUANT && p.group_lanes) {  // per group: no block reduction, lanes of a group combine
+#pragma unroll
+    for (int k = 0; k < PPT; ++k) {
+      const int pk = pk_begin + (int)threadIdx.x + k * (int)blockDim.x;
+      float yr[8];
+      unpack8<DT>(y[k], yr);
+      const uint2 cw = quant_pack_per_group(yr, p.group_lanes, valid[k],
+                                            p.scale + row * (int64_t)p.ngroups + pk / p.group_lanes);
+      if (!valid[k]) continue;
+      const int64_t e0 = row_e + (int64_t)pk * 8;
+      if constexpr (VEC) {
+        st_v2(p.q + e0, cw);
+      } else {
+        const uint32_t c2[2] = {cw.x, cw.y};
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (e0 + i < row_end) st_u8(p.q + e0 + i, (uint8_t)((c2[i >> 2] >> (8 * (i & 3))) & 0xFFu));
+      }
+    }
+  } else if constexpr (QUANT) {
     float am = block_allreduce<true>(amax, red_amax);
     if (csize > 1) {
       if (threadIdx.x == 0) slot_amax = am;

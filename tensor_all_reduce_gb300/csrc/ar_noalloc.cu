@@ -100,7 +100,7 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_noalloc(const ar_fused_args* a, voi
   const ar_status st = setup_current_device(dev, &ds);
   if (st != AR_OK) return st;
 
-  const bool quant = a->quant == AR_QUANT_FP8_E4M3_PER_TOKEN;
+  const bool quant = a->quant != AR_QUANT_NONE;
   const int es = 2;
   const int row_packs = (int)(a->h / 8);
   const int rows_per_stage = a->n + (a->residual_in ? 1 : 0);
@@ -131,6 +131,8 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_noalloc(const ar_fused_args* a, voi
   p.gemma = a->gemma != 0;
   p.skip_norm = a->skip_norm != 0;
   p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
+  p.group_lanes = a->quant == AR_QUANT_FP8_E4M3_PER_GROUP ? a->group_size / 8 : 0;
+  p.ngroups = a->quant == AR_QUANT_FP8_E4M3_PER_GROUP ? (int)(a->h / a->group_size) : 0;
   ar::StagedParams sp;
   sp.stages = S;
   sp.row_bytes = (int)(a->h * es);

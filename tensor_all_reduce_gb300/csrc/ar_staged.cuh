@@ -244,7 +244,15 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
       for (int k = 0; k < PPT; ++k)
         if (valid[k]) st_v4(static_cast<uint16_t*>(p.out) + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8, y[k]);
     }
-    if constexpr (QUANT) {
+    if (QUANT && p.group_lanes) {  // per group: lanes of a group combine, no block reduction
+#pragma unroll
+      for (int k = 0; k < PPT; ++k) {
+        const int pk = (int)threadIdx.x + k * (int)blockDim.x;
+        const uint2 cw = quant_pack_per_group(zf[k], p.group_lanes, valid[k],
+                                              p.scale + row * (int64_t)p.ngroups + pk / p.group_lanes);
+        if (valid[k]) st_v2(p.q + row_e + (int64_t)pk * 8, cw);
+      }
+    } else if constexpr (QUANT) {
       const float am = block_allreduce<true>(amax, red_amax[i & 1]);
       const float scale = __fdiv_rn(am, 448.0f);
       if (threadIdx.x == 0) st_f32(p.scale + row, scale);

@@ -82,6 +82,7 @@ class FusedWorkload:
     seed: int = 1234
     skip_norm: bool = False      # all-reduce (+ residual) + per-token FP8 without RMSNorm
     out_fp32: bool = False       # the normed output stored as fp32
+    group: int = 0               # per-group FP8 with this many elements per group (0: per token)
 
     def inputs(self) -> Dict[str, object]:
         return fused_inputs(self.n, self.m, self.h, self.dtype, self.seed, self.gemma, self.residual)
@@ -97,7 +98,7 @@ class FusedWorkload:
         if self.mirror or not self.quant:
             total += mh * (4 if self.out_fp32 else b)
         if self.quant:
-            total += mh + 4 * self.m
+            total += mh + 4 * (self.m * (self.h // self.group) if self.group else self.m)
         return total
 
 
@@ -143,10 +144,12 @@ def large_m() -> List[FusedWorkload]:
 
 def options() -> List[FusedWorkload]:
     """The fused path's further forms: all-reduce + residual + per-token FP8 without the norm,
-    and the normalised output in fp32."""
+    the normalised output in fp32, and per-group FP8 (groups of 128)."""
     return [FusedWorkload("n4_m2800_h6144_bf16_nonorm_fp8", 4, 2800, 6144, quant=True, mirror=False,
                           skip_norm=True, seed=1239),
-            FusedWorkload("n4_m2800_h6144_bf16_f32out", 4, 2800, 6144, out_fp32=True, seed=1240)]
+            FusedWorkload("n4_m2800_h6144_bf16_f32out", 4, 2800, 6144, out_fp32=True, seed=1240),
+            FusedWorkload("n4_m2800_h6144_bf16_gemma_fp8_group128", 4, 2800, 6144, gemma=True, quant=True,
+                          mirror=True, group=128, seed=1241)]
 
 
 def all_fused() -> List[FusedWorkload]:

@@ -132,8 +132,19 @@ def test_fused_validation(lib):
     # fp32 output: 4-byte alignment, and never an alias of a 16-bit input
     assert fused(out_fp32=True, out=BASE + 7 * 64 * MB + 2) == AL
     assert fused(out_fp32=True, m=8) == NI
+    # per-group FP8: a power-of-two group of 8..256 elements that divides h, rows <= 8192
+    QG = dict(quant=True, q_out=BASE + 8 * 64 * MB, scale_out=BASE + 9 * 64 * MB)
+    assert fused(group_size=128, **QG) == NI
+    assert fused(group_size=100, **QG) == IA
+    assert fused(group_size=512, **QG) == IA
+    assert fused(group_size=4, **QG) == IA
+    assert fused(group_size=128, h=6144 + 64, **QG) == IA
+    assert fused(group_size=128, h=16384, m=4, **QG) == tar.AR_ERR_UNSUPPORTED
     OV = tar.AR_ERR_OVERLAP
     assert fused(out_fp32=True, out=BASE) == OV                          # fp32 y over partials[0]
+    # the per-group scales are m * h / G floats: these would run into the codes
+    assert fused(group_size=8, quant=True, q_out=BASE + 8 * 64 * MB + 16 * 6144 // 8 * 4 - 4,
+                 scale_out=BASE + 8 * 64 * MB) == OV
     assert fused(out=BASE + 32) == OV                                   # inside partials[0]
     assert fused(residual_out=BASE + 7 * 64 * MB) == OV                 # residual_out == out
     assert fused(out=BASE + 6 * 64 * MB) == OV                          # out on the weight

@@ -112,7 +112,10 @@ def test_skip_norm_fp32_output_is_z(ctx, dev, orc):
     assert np.array_equal(y32.cpu().numpy(), z)
 
 
-@pytest.mark.parametrize("wl", synth.options(), ids=[w.name for w in synth.options()])
+OPTION_WORKLOADS = [w for w in synth.options() if not w.group]   # per-group: test_gpu_groupquant.py
+
+
+@pytest.mark.parametrize("wl", OPTION_WORKLOADS, ids=[w.name for w in OPTION_WORKLOADS])
 def test_option_workloads_full_size(ctx, dev, orc, wl):
     _set(ctx, {})
     inp = wl.inputs()
