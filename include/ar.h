@@ -106,9 +106,9 @@ ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int
                         ar_dtype dtype, void* stream);
 
 /*
- * Arguments of the fused call.  All arrays are contiguous row-major; a row is h elements
- * (padded or strided rows are not part of this contract: [P1] Changes sends them to the
- * unfused path).  Counterpart of
+ * Arguments of the fused call.  Arrays are row-major with rows of h elements; rows may be
+ * padded (row strides ld_in / ld_out; [P1] Changes sends padded or strided rows to the
+ * unfused path, here they stay fused).  Counterpart of
  * tensor_model_parallel_fused_allreduce_rmsnorm(x, res, w, eps, gemma_norm=) and of the
  * unfused rmsnorm2d_fwd_with_add(out, x, res, res_out, w, eps, gemma, 0) ([P1] the
  * bench_ar_rms.py listing).
@@ -140,6 +140,12 @@ typedef struct {
                                               quantises the dtype-rounded row) */
   int group_size;                          /* per-group FP8: 8, 16, 32, 64, 128 or 256 elements,
                                               dividing h, with h <= 8192; ignored otherwise */
+  int64_t ld_in;                           /* elements between the starts of consecutive rows of
+                                              the partials and residual_in; 0 means h (contiguous),
+                                              else >= h (padded or strided rows) */
+  int64_t ld_out;                          /* the same for residual_out, out and q_out; 0 means h.
+                                              Strides that keep rows 16-byte aligned (multiples of 8)
+                                              take the vector kernels, others the element-wise ones */
 } ar_fused_args;
 
 /*
@@ -152,8 +158,8 @@ typedef struct {
  * with quant, scale_out[row] = amax / 448 (fp32) and q_out = e4m3(y / scale), with an
  * all-zero row giving scale 0 and codes 0.  E4M3 is the OCP "fn" format (max 448).
  * Aliasing: residual_out and out may each be EXACTLY one of the [m, h] inputs
- * (residual_in or a partial), because every element is read before the same thread
- * writes it; any other overlap between an output and an input, or between two outputs,
+ * (residual_in or a partial) when ld_in and ld_out give the same stride, because every
+ * element is read before the same thread writes it; any other overlap between an output and an input, or between two outputs,
  * is refused with AR_ERR_OVERLAP before anything is launched.
  */
 ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* args, void* stream);

@@ -67,6 +67,8 @@ class ArFusedArgs(ctypes.Structure):
         ("skip_norm", ctypes.c_int),
         ("out_fp32", ctypes.c_int),
         ("group_size", ctypes.c_int),
+        ("ld_in", ctypes.c_int64),
+        ("ld_out", ctypes.c_int64),
     ]
 
 
@@ -201,7 +203,8 @@ def ar_fused_reduce_rmsnorm_batch(ctx: int, calls: Sequence[ArFusedArgs], stream
 def make_fused_args(partials: Sequence[int], residual_in: Optional[int], residual_out: Optional[int],
                     weight: Optional[int], out: Optional[int], eps: float, gemma: bool, quant: bool,
                     q_out: Optional[int], scale_out: Optional[int], m: int, h: int, dtype: int,
-                    skip_norm: bool = False, out_fp32: bool = False, group_size: int = 0) -> ArFusedArgs:
+                    skip_norm: bool = False, out_fp32: bool = False, group_size: int = 0,
+                    ld_in: int = 0, ld_out: int = 0) -> ArFusedArgs:
     a = ArFusedArgs()
     a.n = len(partials)
     for i, p in enumerate(partials):
@@ -214,6 +217,8 @@ def make_fused_args(partials: Sequence[int], residual_in: Optional[int], residua
     a.gemma = int(bool(gemma))
     a.quant = (AR_QUANT_FP8_E4M3_PER_GROUP if group_size else AR_QUANT_FP8_E4M3_PER_TOKEN) if quant else AR_QUANT_NONE
     a.group_size = int(group_size)
+    a.ld_in = int(ld_in)
+    a.ld_out = int(ld_out)
     a.q_out = q_out
     a.scale_out = scale_out
     a.m = m
@@ -240,6 +245,22 @@ def _stream(stream) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
     return stream.cuda_stream
+
+
+def _row_stride(tensors, m, h, dtype, what) -> int:
+    """The common row stride (in elements) of [m, h] CUDA tensors with unit column stride."""
+    ld = None
+    for t in tensors:
+        if t is None:
+            continue
+        if t.shape != (m, h) or not t.is_cuda or (dtype is not None and t.dtype != dtype) or \
+                (h > 1 and t.stride(1) != 1) or (m > 1 and t.stride(0) < h):
+            raise ValueError(f"{what} must be [m, h] CUDA tensors with unit column stride")
+        s = t.stride(0) if m > 1 else h
+        if ld is not None and s != ld:
+            raise ValueError(f"{what} must share one row stride")
+        ld = s
+    return h if ld is None else ld
 
 
 class Context:
@@ -297,17 +318,22 @@ class Context:
                              want_out: bool = True, want_residual_out: bool = True, stream=None,
                              skip_norm: bool = False, out_fp32: bool = False, group_size: int = 0):
         """Returns (out, residual_out, q_out, scale_out); absent outputs are None.  With
-        skip_norm there is no RMSNorm (weight may be None); with out_fp32 `out` is float32."""
+        skip_norm there is no RMSNorm (weight may be None); with out_fp32 `out` is float32.
+        Inputs (and given outputs) may have padded rows: unit column stride, one row stride
+        for the inputs and one for the outputs; allocated outputs are contiguous."""
         import torch
         x0 = partials[0]
         m, h = x0.shape
-        for p in list(partials) + ([residual] if residual is not None else []):
-            if p.shape != (m, h) or p.dtype != x0.dtype or not p.is_contiguous() or not p.is_cuda:
-                raise ValueError("partials and residual must be contiguous [m, h] CUDA tensors of one dtype")
+        ld_in = _row_stride([*partials, residual], m, h, x0.dtype, "partials and residual")
+        given = [t for t in (out, residual_out, q_out) if t is not None]
+        ld_out = _row_stride(given, m, h, None, "outputs") if given else h
+        if ld_out != h and ((out is None and (want_out or not quant)) or (residual_out is None and want_residual_out)
+                            or (quant and q_out is None)):
+            raise ValueError("with padded outputs every output must be given")
         if out is None and (want_out or not quant):
             out = torch.empty((m, h), dtype=torch.float32 if out_fp32 else x0.dtype, device=x0.device)
         if residual_out is None and want_residual_out:
-            residual_out = torch.empty_like(x0)
+            residual_out = torch.empty((m, h), dtype=x0.dtype, device=x0.device)
         if quant:
             if q_out is None:
                 q_out = torch.empty((m, h), dtype=torch.uint8, device=x0.device)
@@ -317,7 +343,7 @@ class Context:
         args = make_fused_args([p.data_ptr() for p in partials], _ptr(residual), _ptr(residual_out),
                                _ptr(weight), _ptr(out), eps, gemma, quant, _ptr(q_out), _ptr(scale_out),
                                m, h, _torch_dtype_code(x0), skip_norm=skip_norm, out_fp32=out_fp32,
-                               group_size=group_size)
+                               group_size=group_size, ld_in=ld_in, ld_out=ld_out)
         ar_fused_reduce_rmsnorm(self.handle, args, _stream(stream))
         return out, residual_out, q_out, scale_out
 
@@ -345,10 +371,14 @@ class Context:
                 q = q if q is not None else torch.empty((m, h), dtype=torch.uint8, device=x0.device)
                 sc = sc if sc is not None else torch.empty((m, h // g) if g else (m,), dtype=torch.float32,
                                                            device=x0.device)
+            ld_in = _row_stride([*c["partials"], c.get("residual")], m, h, x0.dtype, "partials and residual")
+            outs = [t for t in (out, ro, q) if t is not None]
+            ld_out = _row_stride(outs, m, h, None, "outputs") if outs else h
             args.append(make_fused_args([p.data_ptr() for p in c["partials"]], _ptr(c.get("residual")), _ptr(ro),
                                         _ptr(c.get("weight")), _ptr(out), c.get("eps", 1e-6), c.get("gemma", False),
                                         quant, _ptr(q), _ptr(sc), m, h, _torch_dtype_code(x0),
-                                        skip_norm=c.get("skip_norm", False), out_fp32=out_fp32, group_size=g))
+                                        skip_norm=c.get("skip_norm", False), out_fp32=out_fp32, group_size=g,
+                                        ld_in=ld_in, ld_out=ld_out))
             results.append((out, ro, q, sc))
         ar_fused_reduce_rmsnorm_batch(self.handle, args, _stream(stream))
         return results

@@ -401,7 +401,11 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   }
   const int64_t scale_count = per_group ? a->m * (a->h / a->group_size) : a->m;
   if (!(a->eps >= 0.0f) || isinf(a->eps)) return AR_ERR_INVALID_ARG;  // also rejects NaN
-  if (a->h > (int64_t)1 << 30 || a->m > ((int64_t)1 << 40) / a->h) return AR_ERR_INVALID_ARG;
+  if (a->h > (int64_t)1 << 30 || a->ld_in < 0 || a->ld_out < 0 || (a->ld_in && a->ld_in < a->h) ||
+      (a->ld_out && a->ld_out < a->h) || a->ld_in > (int64_t)1 << 31 || a->ld_out > (int64_t)1 << 31)
+    return AR_ERR_INVALID_ARG;
+  const int64_t li = a->ld_in ? a->ld_in : a->h, lo = a->ld_out ? a->ld_out : a->h;  // row strides
+  if (a->m > ((int64_t)1 << 40) / (li > lo ? li : lo)) return AR_ERR_INVALID_ARG;
   if (a->m == 0) {  // no rows: only the weight is a real buffer; nothing is touched
     if (!ctx) return AR_ERR_NOT_INITIALIZED;
     ctx->last_variant = "none";
@@ -415,16 +419,18 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   const int es = elem_size(a->dtype);
   const int oes = a->out_fp32 ? 4 : es;  // element size of `out`
   const int64_t mh = a->m * a->h;
-  const int64_t tb = mh * es;  // bytes of one [m, h] tensor
+  const int64_t ext_in = (a->m - 1) * li + a->h;   // elements an input spans (padding included)
+  const int64_t ext_out = (a->m - 1) * lo + a->h;  // elements an output spans
+  const int64_t tb = ext_in * es;                  // bytes of one input [m, h] tensor
   // element alignment
   for (int r = 0; r < a->n; ++r)
     if (!aligned(a->partials[r], es)) return AR_ERR_ALIGNMENT;
   if ((a->residual_in && !aligned(a->residual_in, es)) || (a->residual_out && !aligned(a->residual_out, es)) ||
       !aligned(a->weight, es) || (a->out && !aligned(a->out, oes)) || (quant && !aligned(a->scale_out, 4)))
     return AR_ERR_ALIGNMENT;
-  // overlap: outputs may equal an [m, h] input of the same type exactly (every element is
-  // read before the same thread writes it), never partially overlap an input, and never
-  // overlap one another
+  // overlap: outputs may equal an [m, h] input of the same type and row stride exactly
+  // (every element is read before the same thread writes it), never partially overlap an
+  // input, and never overlap one another
   struct Range { const void* p; int64_t n; bool same_shape; };
   Range ins[AR_MAX_PARTIALS + 2];
   int ni = 0;
@@ -433,10 +439,10 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   if (a->weight) ins[ni++] = {a->weight, (int64_t)a->h * es, false};
   Range outs[4];
   int no = 0;
-  if (a->residual_out) outs[no++] = {a->residual_out, tb, true};
-  if (a->out) outs[no++] = {a->out, mh * oes, !a->out_fp32};
+  if (a->residual_out) outs[no++] = {a->residual_out, ext_out * es, li == lo};
+  if (a->out) outs[no++] = {a->out, ext_out * oes, !a->out_fp32 && li == lo};
   if (quant) {
-    outs[no++] = {a->q_out, mh, false};
+    outs[no++] = {a->q_out, ext_out, false};
     outs[no++] = {a->scale_out, scale_count * 4, false};
   }
   for (int o = 0; o < no; ++o) {
@@ -450,7 +456,9 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   if (!ctx) return AR_ERR_NOT_INITIALIZED;
 
   // ---- variant selection ----
-  bool vec = (a->h % 8) == 0;
+  // the vector kernels need 16-byte-aligned rows: h, and both row strides, multiples of 8
+  bool vec = (a->h % 8) == 0 && (li % 8) == 0 && (lo % 8) == 0;
+  (void)mh;
   for (int r = 0; r < a->n; ++r) vec = vec && aligned(a->partials[r], 16);
   vec = vec && (!a->residual_in || aligned(a->residual_in, 16)) && (!a->residual_out || aligned(a->residual_out, 16)) &&
         aligned(a->weight, 16) && (!a->out || aligned(a->out, 16)) && (!quant || aligned(a->q_out, 8));
@@ -500,6 +508,8 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
     p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
     p.group_lanes = per_group ? a->group_size / 8 : 0;
     p.ngroups = per_group ? (int)(a->h / a->group_size) : 0;
+    p.ld_in = li;
+    p.ld_out = lo;
     ar::StagedParams sp;
     sp.stages = S;
     sp.row_bytes = (int)(a->h * es);
@@ -571,6 +581,8 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
   p.group_lanes = per_group ? a->group_size / 8 : 0;
   p.ngroups = per_group ? (int)(a->h / a->group_size) : 0;
+  p.ld_in = li;
+  p.ld_out = lo;
 
   const void* fn = a->dtype == AR_DTYPE_BF16 ? ar::fused_kernel_bf16(a->n, ppt, quant, vec)
                                              : ar::fused_kernel_f16(a->n, ppt, quant, vec);
@@ -603,11 +615,13 @@ struct CallRanges {
 
 CallRanges ranges_of(const ar_fused_args* a) {
   CallRanges r;
-  const int64_t es = elem_size(a->dtype), mh = a->m * a->h, tb = mh * es;
+  const int64_t li = a->ld_in ? a->ld_in : a->h, lo = a->ld_out ? a->ld_out : a->h;
+  const int64_t es = elem_size(a->dtype), mh = a->m > 0 ? (a->m - 1) * lo + a->h : 0;
+  const int64_t tb = a->m > 0 ? ((a->m - 1) * li + a->h) * es : 0;
   for (int k = 0; k < a->n; ++k) { r.in[r.nin] = a->partials[k]; r.in_n[r.nin++] = tb; }
   if (a->residual_in) { r.in[r.nin] = a->residual_in; r.in_n[r.nin++] = tb; }
   if (a->weight && !a->skip_norm) { r.in[r.nin] = a->weight; r.in_n[r.nin++] = a->h * es; }
-  if (a->residual_out) { r.out[r.nout] = a->residual_out; r.out_n[r.nout++] = tb; }
+  if (a->residual_out) { r.out[r.nout] = a->residual_out; r.out_n[r.nout++] = mh * es; }
   if (a->out) { r.out[r.nout] = a->out; r.out_n[r.nout++] = mh * (a->out_fp32 ? 4 : es); }
   if (a->quant) {
     const int64_t ns = a->quant == AR_QUANT_FP8_E4M3_PER_GROUP ? a->m * (a->h / a->group_size) : a->m;
@@ -654,7 +668,7 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_batch(ar_ctx* ctx, const ar_fused_a
   int max_row_packs = 1;
   for (int i = 0; i < count; ++i) {
     const ar_fused_args& a = calls[i];
-    bool vec = (a.h % 8) == 0 && a.h <= 8192;
+    bool vec = (a.h % 8) == 0 && a.h <= 8192 && (a.ld_in % 8) == 0 && (a.ld_out % 8) == 0;
     for (int r = 0; r < a.n; ++r) vec = vec && aligned(a.partials[r], 16);
     vec = vec && aligned(a.residual_in, 16) && aligned(a.residual_out, 16) && aligned(a.weight, 16) &&
           aligned(a.out, 16) && (!a.quant || aligned(a.q_out, 8));
@@ -707,6 +721,8 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_batch(ar_ctx* ctx, const ar_fused_a
     p.out_f32 = a.out_fp32 != 0 && a.out != nullptr;
     p.group_lanes = a.quant == AR_QUANT_FP8_E4M3_PER_GROUP ? a.group_size / 8 : 0;
     p.ngroups = a.quant == AR_QUANT_FP8_E4M3_PER_GROUP ? (int)(a.h / a.group_size) : 0;
+    p.ld_in = a.ld_in;
+    p.ld_out = a.ld_out;
     bp.row_start[i] = acc;
     acc += a.m;
   }

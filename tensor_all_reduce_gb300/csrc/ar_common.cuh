@@ -46,6 +46,8 @@ struct FusedParams {
   int out_f32;       // 1: `out` holds fp32 values of y before their rounding
   int group_lanes;   // per-group FP8: lanes (packs) per group, group / 8; 0: per-token FP8
   int ngroups;       // per-group FP8: groups per row, h / group
+  int64_t ld_in;     // elements between row starts of the partials and residual_in (0: h)
+  int64_t ld_out;    // elements between row starts of residual_out, out and q (0: h)
 };
 
 // ---------------------------------------------------------------------------

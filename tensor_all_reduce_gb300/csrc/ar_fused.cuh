@@ -85,8 +85,11 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
   const int64_t row = blockIdx.x / (unsigned)csize;
   const int pk_begin = crank * p.chunk_packs;
   const int pk_end = min(pk_begin + p.chunk_packs, p.row_packs);
-  const int64_t row_e = row * (int64_t)p.h;   // first element of the row
-  const int64_t row_end = row_e + p.h;         // one past the row's last element
+  // rows may be padded: inputs and outputs have their own row strides (0 means h)
+  const int64_t row_i = row * (p.ld_in ? p.ld_in : (int64_t)p.h);     // first input element of the row
+  const int64_t row_i_end = row_i + p.h;
+  const int64_t row_e = row * (p.ld_out ? p.ld_out : (int64_t)p.h);   // first output element of the row
+  const int64_t row_end = row_e + p.h;         // one past the row's last output element
 
   // ---- phase 1: loads of every pack this thread owns, then the reduction --------------
   // Indices of packs beyond the chunk are clamped to the chunk's first pack so that all
@@ -100,8 +103,8 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
     const int pk = pk_begin + (int)threadIdx.x + k * (int)blockDim.x;
     valid[k] = pk < pk_end;
     const int pkc = valid[k] ? pk : pk_begin;
-    const int64_t e0 = row_e + (int64_t)pkc * 8;
-    const int64_t lim = valid[k] ? row_end : row_e;  // scalar variant: nothing for clamped packs
+    const int64_t e0 = row_i + (int64_t)pkc * 8;
+    const int64_t lim = valid[k] ? row_i_end : row_i;  // scalar variant: nothing for clamped packs
     float acc[8];
     load_pack<DT, VEC, true>(p.x[0], e0, lim, acc);
 #pragma unroll

@@ -84,7 +84,7 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_noalloc(const ar_fused_args* a, voi
   if (a->m == 0) return AR_OK;
 
   // Only the staged kernel has this form: 16-byte-aligned rows of at most 8192 elements.
-  bool vec = (a->h % 8) == 0 && a->h <= 8192;
+  bool vec = (a->h % 8) == 0 && a->h <= 8192 && (a->ld_in % 8) == 0 && (a->ld_out % 8) == 0;
   for (int r = 0; r < a->n; ++r) vec = vec && aligned16(a->partials[r]);
   vec = vec && aligned16(a->residual_in) && aligned16(a->residual_out) && aligned16(a->weight) &&
         aligned16(a->out) && (a->quant == AR_QUANT_NONE || (reinterpret_cast<uintptr_t>(a->q_out) % 8) == 0);
@@ -133,6 +133,8 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_noalloc(const ar_fused_args* a, voi
   p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
   p.group_lanes = a->quant == AR_QUANT_FP8_E4M3_PER_GROUP ? a->group_size / 8 : 0;
   p.ngroups = a->quant == AR_QUANT_FP8_E4M3_PER_GROUP ? (int)(a->h / a->group_size) : 0;
+  p.ld_in = a->ld_in;
+  p.ld_out = a->ld_out;
   ar::StagedParams sp;
   sp.stages = S;
   sp.row_bytes = (int)(a->h * es);

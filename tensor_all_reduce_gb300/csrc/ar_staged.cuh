@@ -119,7 +119,7 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
   auto issue = [&](int s, int64_t row) {
     uint8_t* dst = stage_mem + (size_t)s * stage_bytes;
     mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
-    const size_t off = (size_t)row * row_bytes;
+    const size_t off = (size_t)row * (size_t)(p.ld_in ? p.ld_in : (int64_t)p.h) * 2;  // padded rows
 #pragma unroll
     for (int r = 0; r < N; ++r) bulk_g2s(dst + (size_t)r * row_bytes, (const uint8_t*)p.x[r] + off, row_bytes, &full_bar[s]);
     if (has_res) bulk_g2s(dst + (size_t)N * row_bytes, (const uint8_t*)p.res_in + off, row_bytes, &full_bar[s]);
@@ -166,7 +166,7 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
       return;
     }
     const uint8_t* st = stage_mem + (size_t)s * stage_bytes;
-    const int64_t row_e = row * (int64_t)p.h;
+    const int64_t row_e = row * (p.ld_out ? p.ld_out : (int64_t)p.h);  // first output element
 
     uint4 z[PPT];      // rounded residual sum, packed (stored as residual_out)
     float zf[PPT][8];  // the same values as floats

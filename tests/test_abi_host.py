@@ -140,8 +140,19 @@ def test_fused_validation(lib):
     assert fused(group_size=4, **QG) == IA
     assert fused(group_size=128, h=6144 + 64, **QG) == IA
     assert fused(group_size=128, h=16384, m=4, **QG) == tar.AR_ERR_UNSUPPORTED
+    # padded rows: strides of at least h
+    assert fused(ld_in=6144 + 64, ld_out=6144 + 8) == NI
+    assert fused(ld_in=6000) == IA
+    assert fused(ld_out=100) == IA
+    assert fused(ld_in=-8) == IA
     OV = tar.AR_ERR_OVERLAP
     assert fused(out_fp32=True, out=BASE) == OV                          # fp32 y over partials[0]
+    # an output on an input is allowed only with the same row stride
+    assert fused(out=BASE, ld_in=6144 + 64, ld_out=6144 + 64) == NI
+    assert fused(out=BASE, ld_in=6144 + 64, ld_out=6144) == OV
+    # strided extents count: residual_out's 16 rows with stride 4.5M elements span 135 MB
+    # and reach `out`, 128 MB further on
+    assert fused(ld_out=4_500_000) == OV
     # the per-group scales are m * h / G floats: these would run into the codes
     assert fused(group_size=8, quant=True, q_out=BASE + 8 * 64 * MB + 16 * 6144 // 8 * 4 - 4,
                  scale_out=BASE + 8 * 64 * MB) == OV
