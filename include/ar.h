@@ -241,10 +241,16 @@ typedef enum {
   AR_OPT_PACKS_PER_THREAD = 2, /* 0 auto, else 1, 2 or 4 16-byte packs per thread */
   AR_OPT_REDUCE_UNROLL = 3,  /* 0 auto, else 1, 2 or 4 packs per thread per tile */
   AR_OPT_STAGES = 4,         /* 0 auto, else 1..4 shared-memory stages per CTA (staged variant) */
-  AR_OPT_PDL = 5             /* 1 (the default): launch with programmatic dependent launch, so
+  AR_OPT_PDL = 5,            /* 1 (the default): launch with programmatic dependent launch, so
                                 a kernel may be scheduled while its predecessor on the stream
                                 still runs (every kernel here waits for its predecessors to
                                 complete before it reads memory); 0: ordinary stream order */
+  AR_OPT_WAIT_CYCLES = 6,    /* bound of one staged-kernel wait in SM clock cycles (1e3..8e9);
+                                0 (the default): 2e9, about a second */
+  AR_OPT_TEST_STALL = 7      /* test hook, 0 (the default) or 1: the staged kernels arm each CTA's
+                                first stage without issuing its copies, so that wait runs out and
+                                the call ends early with code 1 in the status word (exercises the
+                                failure path; outputs are then incomplete) */
 } ar_option;
 ar_status ar_set_option(ar_ctx* ctx, ar_option opt, int64_t value);
 

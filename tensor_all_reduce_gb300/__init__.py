@@ -40,6 +40,8 @@ AR_OPT_PACKS_PER_THREAD = 2
 AR_OPT_REDUCE_UNROLL = 3
 AR_OPT_STAGES = 4
 AR_OPT_PDL = 5
+AR_OPT_WAIT_CYCLES = 6
+AR_OPT_TEST_STALL = 7
 VARIANT_AUTO, VARIANT_ROW, VARIANT_CLUSTER, VARIANT_STAGED, VARIANT_SCALAR = 0, 1, 2, 3, 4
 
 AR_INFO_SM_COUNT = 0

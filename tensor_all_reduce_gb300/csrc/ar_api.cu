@@ -28,6 +28,8 @@ struct ar_ctx {
   int reduce_unroll;
   int stages;
   int pdl;               // launch with programmatic stream serialisation
+  long long wait_cycles; // bound of one staged-kernel wait (0: about a second)
+  int test_stall;        // test hook: make the staged kernel's first waits run out
   const char* last_variant;
   char last_error[256];
 };
@@ -298,6 +300,14 @@ ar_status ar_set_option(ar_ctx* ctx, ar_option opt, int64_t v) {
       if (v != 0 && v != 1) return AR_ERR_INVALID_ARG;
       ctx->pdl = (int)v;
       return AR_OK;
+    case AR_OPT_WAIT_CYCLES:
+      if (v != 0 && (v < 1000 || v > 8000000000LL)) return AR_ERR_INVALID_ARG;
+      ctx->wait_cycles = v;
+      return AR_OK;
+    case AR_OPT_TEST_STALL:
+      if (v != 0 && v != 1) return AR_ERR_INVALID_ARG;
+      ctx->test_stall = (int)v;
+      return AR_OK;
   }
   return AR_ERR_INVALID_ARG;
 }
@@ -510,11 +520,12 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
     p.ngroups = per_group ? (int)(a->h / a->group_size) : 0;
     p.ld_in = li;
     p.ld_out = lo;
-    ar::StagedParams sp;
+    ar::StagedParams sp = {};
     sp.stages = S;
     sp.row_bytes = (int)(a->h * es);
     sp.err = ctx->d_status;
-    sp.wait_cycles = 2000000000LL;  // about one second at the SM clock
+    sp.wait_cycles = ctx->wait_cycles ? ctx->wait_cycles : 2000000000LL;  // about a second at 2 GHz
+    sp.stall_first = ctx->test_stall;
     const void* fn = a->dtype == AR_DTYPE_BF16 ? ar::staged_kernel_bf16(a->n, sppt, quant)
                                                : ar::staged_kernel_f16(a->n, sppt, quant);
     if (!fn) return AR_ERR_UNSUPPORTED;
@@ -697,7 +708,8 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_batch(ar_ctx* ctx, const ar_fused_a
   bp.count = count;
   bp.sp.stages = 1;
   bp.sp.err = ctx->d_status;
-  bp.sp.wait_cycles = 2000000000LL;
+  bp.sp.wait_cycles = ctx->wait_cycles ? ctx->wait_cycles : 2000000000LL;
+  bp.sp.stall_first = ctx->test_stall;
   int64_t acc = 0;
   for (int i = 0; i < count; ++i) {
     const ar_fused_args& a = calls[i];

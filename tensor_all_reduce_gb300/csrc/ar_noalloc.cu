@@ -135,7 +135,7 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_noalloc(const ar_fused_args* a, voi
   p.ngroups = a->quant == AR_QUANT_FP8_E4M3_PER_GROUP ? (int)(a->h / a->group_size) : 0;
   p.ld_in = a->ld_in;
   p.ld_out = a->ld_out;
-  ar::StagedParams sp;
+  ar::StagedParams sp = {};
   sp.stages = S;
   sp.row_bytes = (int)(a->h * es);
   sp.err = ds.scratch;

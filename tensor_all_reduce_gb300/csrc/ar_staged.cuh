@@ -32,6 +32,8 @@ struct StagedParams {
   int row_bytes;          // h * 2
   int* err;               // device status word (0 = fine), written only on a timeout
   long long wait_cycles;  // bound of one mbarrier wait
+  int stall_first;        // test hook: arm each CTA's first stage without issuing its copies, so
+                          // that wait runs out (the failure path runs without any fault)
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
@@ -119,6 +121,7 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
   auto issue = [&](int s, int64_t row) {
     uint8_t* dst = stage_mem + (size_t)s * stage_bytes;
     mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
+    if (sp.stall_first && row == first) return;  // nothing will complete this phase
     const size_t off = (size_t)row * (size_t)(p.ld_in ? p.ld_in : (int64_t)p.h) * 2;  // padded rows
 #pragma unroll
     for (int r = 0; r < N; ++r) bulk_g2s(dst + (size_t)r * row_bytes, (const uint8_t*)p.x[r] + off, row_bytes, &full_bar[s]);
