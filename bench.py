@@ -273,19 +273,21 @@ def time_graph(sets, ctx, calls: int, steps: int, warmup: int, world: int, sampl
     torch.cuda.synchronize()
     barrier(world)
     torch.cuda.synchronize()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # one event between consecutive replays: the total and every step's own duration
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
     t0 = time.time()
-    start.record()
-    for _ in range(steps):
+    evs[0].record()
+    for i in range(steps):
         g.replay()
-    end.record()
-    end.synchronize()
+        evs[i + 1].record()
+    evs[-1].synchronize()
     t1 = time.time()
     torch.cuda.synchronize()
     barrier(world)
-    elapsed_ms = start.elapsed_time(end)
+    elapsed_ms = evs[0].elapsed_time(evs[-1])
+    step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(steps)]
     del g
-    return elapsed_ms, t0, t1
+    return elapsed_ms, t0, t1, step_ms
 
 
 def e2e_fused(ctx, wl, steps: int, dev):
@@ -353,14 +355,56 @@ def oracle_sample_us(wl, rows: int):
     return dt * 1e6 * (wl.m / rows), rows
 
 
+def host_cores() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def oracle_all_cores_us(wl, seconds: float = 4.0, runs: int = 3):
+    """Rows partitioned over every host core: each thread runs the same serial oracle on its own
+    contiguous block of rows (rows are independent; the C call releases the GIL).  Returns
+    (us per full call, threads, rows per run)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    from tensor_all_reduce_gb300 import synth
+    cores = host_cores()
+    us1, _ = oracle_sample_us(wl, 16)
+    per_row_s = us1 / 1e6 / wl.m
+    rows = max(cores, min(wl.m, int(seconds / runs * cores / per_row_s)))
+    inp = synth.fused_inputs(wl.n, rows, wl.h, wl.dtype, seed=wl.seed, gemma=wl.gemma, residual=wl.residual)
+    parts = [synth.bits(p) for p in inp["partials"]]
+    res = synth.bits(inp["residual"]) if inp["residual"] is not None else None
+    w = synth.bits(inp["weight"])
+    orc = oracle.get()
+    bounds = [rows * k // cores for k in range(cores + 1)]
+
+    def block(k):
+        a, b = bounds[k], bounds[k + 1]
+        if b > a:
+            orc.fused([p[a:b] for p in parts], None if res is None else res[a:b], w, 1e-6,
+                      wl.gemma, wl.quant, wl.dtype)
+
+    samples = []
+    with ThreadPoolExecutor(cores) as ex:
+        for _ in range(runs):
+            t = time.perf_counter()
+            list(ex.map(block, range(cores)))
+            samples.append((time.perf_counter() - t) * 1e6 * (wl.m / rows))
+    return statistics.median(samples), cores, rows
+
+
 def cpu_baseline(wl, seconds: float = 12.0):
-    """Serial oracle (one thread), timed on a bounded sample of the workload's rows."""
+    """Serial oracle (one thread), timed on a bounded sample of the workload's rows; beside it
+    the same oracle with the rows partitioned over all host cores."""
     us1, rows = oracle_sample_us(wl, 16)                 # size the sample
     per_row_s = us1 / 1e6 / wl.m
     rows = max(16, min(wl.m, int(seconds / 3 / per_row_s)))
     samples = [oracle_sample_us(wl, rows)[0] for _ in range(3)]
+    mt_us, cores, mt_rows = oracle_all_cores_us(wl)
     return {"value": statistics.median(samples), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"serial C oracle on {rows} of {wl.m} rows, median of 3 runs, scaled to a full call"}
+            "sample": f"serial C oracle on {rows} of {wl.m} rows, median of 3 runs, scaled to a full call",
+            "all_cores": {"value": round(mt_us, 3), "unit": UNIT, "cores": cores,
+                          "sample": f"the same oracle, {mt_rows} of {wl.m} rows split in {cores} row blocks "
+                                    f"over {cores} threads, median of 3 runs, scaled to a full call"}}
 
 
 def run_reference(args, world, rank):
@@ -402,13 +446,13 @@ def sweep(ctx, dev, l2, peak):
         R = rotation_sets(fp, l2)
         calls = max(64, R)
         sets = (FusedSets if fused else ReduceSets)(wl, R, dev)
-        ms, _, _ = time_graph(sets, ctx, calls, steps=5, warmup=2, world=1)
+        ms, *_ = time_graph(sets, ctx, calls, steps=5, warmup=2, world=1)
         cold = ms * 1000 / (5 * calls)
         variant = ctx.last_variant
         del sets
         torch.cuda.empty_cache()
         sets = (FusedSets if fused else ReduceSets)(wl, 1, dev)
-        ms, _, _ = time_graph(sets, ctx, 64, steps=5, warmup=2, world=1)
+        ms, *_ = time_graph(sets, ctx, 64, steps=5, warmup=2, world=1)
         warm = ms * 1000 / (5 * 64)
         del sets
         torch.cuda.empty_cache()
@@ -422,12 +466,12 @@ def sweep(ctx, dev, l2, peak):
     R = rotation_sets(k * wl.algorithmic_bytes(), l2, cap=64)
     for batched in (True, False):
         sets = BatchSets(wl, k, R, dev, batched)
-        ms, _, _ = time_graph(sets, ctx, max(R, 32), steps=5, warmup=2, world=1)
+        ms, *_ = time_graph(sets, ctx, max(R, 32), steps=5, warmup=2, world=1)
         cold = ms * 1000 / (5 * max(R, 32))
         variant = ctx.last_variant
         del sets
         sets = BatchSets(wl, k, 1, dev, batched)
-        ms, _, _ = time_graph(sets, ctx, 32, steps=5, warmup=2, world=1)
+        ms, *_ = time_graph(sets, ctx, 32, steps=5, warmup=2, world=1)
         warm = ms * 1000 / (5 * 32)
         del sets
         torch.cuda.empty_cache()
@@ -478,7 +522,7 @@ def main(argv=None):
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
-    elapsed_ms, t0, t1 = time_graph(sets, ctx, calls, args.steps, args.warmup, world)
+    elapsed_ms, t0, t1, step_ms = time_graph(sets, ctx, calls, args.steps, args.warmup, world)
     clocks = sampler.stop(t0, t1) if sampler else None
     variant = ctx.last_variant
     max_ms = max_over_ranks(elapsed_ms, world, dev)
@@ -514,6 +558,10 @@ def main(argv=None):
                          "peak_kind": peak_kind, "algorithmic_bytes_per_launch": fp},
             "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "note": "one call per step: inputs copied from pinned host memory, outputs copied back"},
+            "per_step": {"median": round(statistics.median(step_ms) * 1000.0 / calls, 3),
+                         "min": round(min(step_ms) * 1000.0 / calls, 3),
+                         "max": round(max(step_ms) * 1000.0 / calls, 3), "unit": UNIT,
+                         "note": "rank 0's replays one by one (CUDA events between replays)"},
             "gpu_launches": launches,
             "clocks": clocks,
         }

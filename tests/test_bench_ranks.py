@@ -74,3 +74,15 @@ def test_reference_arm_under_two_ranks_only_rank0_prints():
     line = lines[0]
     assert line["impl"] == "reference" and line["unit"] == "us/call" and line["higher_is_better"] is False
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_cpu_baseline_reports_serial_and_all_cores():
+    sys.path.insert(0, ROOT)
+    import bench
+    from tensor_all_reduce_gb300 import synth
+    wl = synth.by_name("n4_m16_h6144_bf16_plain")
+    us, cores, rows = bench.oracle_all_cores_us(wl, seconds=0.3, runs=2)
+    assert us > 0 and cores == bench.host_cores() and 1 <= rows <= wl.m
+    cpu = bench.cpu_baseline(wl, seconds=0.3)
+    assert cpu["kind"] == "oracle" and cpu["cores"] == 1 and cpu["value"] > 0
+    assert cpu["all_cores"]["cores"] == cores and cpu["all_cores"]["unit"] == cpu["unit"]
