@@ -249,19 +249,26 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Block-wide sum (MAX=false) or max (MAX=true) returned to every thread.  `buf` holds one
-// float per warp and must not be reused by another reduction before a __syncthreads.
-// Warp totals are combined in warp order, so every thread sees the same value.
+// Block-wide sum (MAX=false) or max (MAX=true) returned to every thread: a butterfly in
+// each warp, one barrier, then a butterfly over the warp totals in every warp.  Both
+// partners of a butterfly step combine the same two operands, so every lane of every warp
+// ends with the same bits.  `buf` holds one float per warp and must not be reused by
+// another reduction before the next barrier.  When `any` is given, `flag` is OR-ed over the
+// block in the same barrier and the result stored there (a caller agrees on a failure at
+// no extra barrier).
 template <bool MAX>
-__device__ __forceinline__ float block_allreduce(float v, float* buf) {
+__device__ __forceinline__ float block_allreduce(float v, float* buf, bool flag = false, bool* any = nullptr) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = (blockDim.x + 31) >> 5;
   v = MAX ? warp_max(v) : warp_sum(v);
   if (lane == 0) buf[warp] = v;
-  __syncthreads();
-  float t = buf[0];
-  for (int i = 1; i < nwarps; ++i) t = MAX ? fmaxf(t, buf[i]) : t + buf[i];
-  return t;
+  if (any != nullptr)
+    *any = __syncthreads_or(flag) != 0;
+  else
+    __syncthreads();
+  // identity of the sum, and of the max of magnitudes (every caller's values are >= 0)
+  const float t = lane < nwarps ? buf[lane] : 0.0f;
+  return MAX ? warp_max(t) : warp_sum(t);
 }
 
 // ---------------------------------------------------------------------------

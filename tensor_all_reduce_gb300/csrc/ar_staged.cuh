@@ -19,7 +19,8 @@
 // barrier sits outside any per-thread predicate.
 //
 // Waits are bounded: a wait on a stage's mbarrier gives up after `wait_cycles` SM clock
-// cycles, the CTA agrees on the failure with __syncthreads_or, records code 1 in `err`,
+// cycles, the CTA agrees on the failure in the row's square-sum barrier (an OR-reduction
+// in the same barrier), records code 1 in `err`,
 // waits (bounded again) for its own copies still in flight, and returns.
 #pragma once
 
@@ -160,14 +161,9 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
     const int64_t row = first + i * stride;
     // Every thread waits on the stage's barrier itself (measured faster than one thread
     // polling and a CTA barrier) and so observes the copy's completion before its reads.
+    // A thread whose wait ran out still reads the stage (in bounds; the values are
+    // discarded): the CTA agrees on the failure in the square-sum's barrier below.
     const bool ok = mbar_wait_bounded(&full_bar[s], parity, sp.wait_cycles);
-    if (__syncthreads_or(!ok)) {
-      if (threadIdx.x == 0) atomicExch(sp.err, 1);
-      // let this CTA's own copies still in flight land before shared memory is released
-      for (int64_t j = i; j < my_rows && j < i + S; ++j)
-        (void)mbar_wait_bounded(&full_bar[j % S], (uint32_t)((j / S) & 1), sp.wait_cycles);
-      return;
-    }
     const uint8_t* st = stage_mem + (size_t)s * stage_bytes;
     const int64_t row_e = row * (p.ld_out ? p.ld_out : (int64_t)p.h);  // first output element
 
@@ -204,10 +200,18 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
       }
     }
     float tot = 0.0f;
+    bool failed;
     if (!p.skip_norm)
-      tot = block_allreduce<false>(ss, red_ss[i & 1]);
+      tot = block_allreduce<false>(ss, red_ss[i & 1], !ok, &failed);
     else
-      __syncthreads();
+      failed = __syncthreads_or(!ok) != 0;
+    if (failed) {
+      if (threadIdx.x == 0) atomicExch(sp.err, 1);
+      // let this CTA's own copies still in flight land before shared memory is released
+      for (int64_t j = i; j < my_rows && j < i + S; ++j)
+        (void)mbar_wait_bounded(&full_bar[j % S], (uint32_t)((j / S) & 1), sp.wait_cycles);
+      return;
+    }
     // every thread has read stage s: refill it with the row S iterations ahead
     if (threadIdx.x == 0 && i + S < my_rows) {
       fence_proxy_async_smem();
