@@ -480,10 +480,10 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   // ---- staged (bulk-copy pipelined, persistent) variant for large batches ----
   const int rows_per_stage = a->n + (a->residual_in ? 1 : 0);
   const int64_t stage_bytes = (int64_t)rows_per_stage * a->h * es;
-  // Stages per CTA: two stages in one CTA per SM stream best, with or without the per-token
-  // FP8 epilogue; per-group FP8 is best with one stage and several CTAs per SM (same-GPU A/B
-  // runs on GB300 at N = 4 and 8, h = 6144 and 7168, m = 1024 .. 4096).
-  int S = ctx->stages ? ctx->stages : (per_group ? 1 : 2);
+  // Stages per CTA: two stages in one CTA per SM stream best with every epilogue (three
+  // stages, or one stage and two CTAs per SM, were slower in same-GPU A/B runs on GB300 at
+  // N = 4 and 8, h = 6144 and 7168, m = 1024 .. 4096).
+  int S = ctx->stages ? ctx->stages : 2;
   if (!ctx->stages && S * stage_bytes > ctx->max_dyn_smem) S = 1;
   const bool staged_ok = vec && row_packs <= 1024 && S * stage_bytes <= ctx->max_dyn_smem;
   // Automatic choice: fewer rows than SMs -> one staged CTA per row (bulk row loads have
@@ -493,8 +493,12 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
                            (a->m < ctx->sm_count || a->m >= 4LL * ctx->sm_count);
   if (ctx->force_variant == 3 || (staged_auto && staged_ok)) {
     if (!staged_ok) return AR_ERR_UNSUPPORTED;
-    // packs per thread: 2 (384 threads for h = 6144)
-    const int sppt = ctx->ppt ? ctx->ppt : 2;
+    // packs per thread: 1 (768 threads for h = 6144) when each CTA runs through many rows
+    // with the norm and at most 4 partials, else 2 (same A/B runs: 1 pack was ~1 % faster on
+    // N = 4, 2800 x 6144 with and without FP8, 2 packs on 1024 rows, on N = 8 and without
+    // the norm)
+    const bool one_pack = a->n <= 4 && !a->skip_norm && a->m >= 8LL * ctx->sm_count && row_packs <= 1024;
+    const int sppt = ctx->ppt ? ctx->ppt : (one_pack ? 1 : 2);
     int sblock = ((row_packs + sppt - 1) / sppt + 31) / 32 * 32;
     if (sblock < 32) sblock = 32;
     ar::FusedParams p;

@@ -105,7 +105,7 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_noalloc(const ar_fused_args* a, voi
   const int row_packs = (int)(a->h / 8);
   const int rows_per_stage = a->n + (a->residual_in ? 1 : 0);
   const int64_t stage_bytes = (int64_t)rows_per_stage * a->h * es;
-  int S = quant ? 1 : 2;
+  int S = 2;  // two stages: the fastest ring with every epilogue
   if (S * stage_bytes > ds.max_dyn_smem) S = 1;
   if (S * stage_bytes > ds.max_dyn_smem) return AR_ERR_UNSUPPORTED;
   const int ppt = 2;

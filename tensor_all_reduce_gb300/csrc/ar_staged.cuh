@@ -97,6 +97,9 @@ __device__ __forceinline__ uint4 lds_v4(const void* p) {
 
 // The rows r = first + i * stride (i = 0, 1, ...) of one call, processed by this CTA
 // through its shared-memory ring.  Shared by the persistent kernel and the batched one.
+//
+// Per row there are one or two block reductions: the square-sum, and with per-token FP8
+// the amax of the rounded output.
 template <int DT, int N, int PPT, bool QUANT>
 __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedParams& sp, int64_t first,
                                             int64_t stride) {
@@ -155,25 +158,20 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
     }
   }
 
-  for (int64_t i = 0; i < my_rows; ++i) {
-    const int s = (int)(i % S);
-    const uint32_t parity = (uint32_t)((i / S) & 1);
-    const int64_t row = first + i * stride;
-    // Every thread waits on the stage's barrier itself (measured faster than one thread
-    // polling and a CTA barrier) and so observes the copy's completion before its reads.
-    // A thread whose wait ran out still reads the stage (in bounds; the values are
-    // discarded): the CTA agrees on the failure in the square-sum's barrier below.
+  auto row_of = [&](int64_t i) { return first + i * stride; };
+  auto out_base = [&](int64_t i) { return row_of(i) * (p.ld_out ? p.ld_out : (int64_t)p.h); };  // first output element
+  auto pack_index = [&](int k) { return (int64_t)((int)threadIdx.x + k * (int)blockDim.x); };
+
+  // Wait for a row's stage s (bounded; `parity` selects the phase), then read it: rounded sum, residual add, this
+  // thread's part of the square-sum.  A thread whose wait ran out still reads the stage
+  // (in bounds; the values are discarded): the CTA agrees on the failure in the next barrier.
+  auto read_row = [&](int s, uint32_t parity, uint4 (&z)[PPT], float (&zf)[PPT][8], float& ss) -> bool {
     const bool ok = mbar_wait_bounded(&full_bar[s], parity, sp.wait_cycles);
     const uint8_t* st = stage_mem + (size_t)s * stage_bytes;
-    const int64_t row_e = row * (p.ld_out ? p.ld_out : (int64_t)p.h);  // first output element
-
-    uint4 z[PPT];      // rounded residual sum, packed (stored as residual_out)
-    float zf[PPT][8];  // the same values as floats
-    float ss = 0.0f;
+    ss = 0.0f;
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
-      const int pk = (int)threadIdx.x + k * (int)blockDim.x;
-      const int pkc = valid[k] ? pk : 0;
+      const int pkc = valid[k] ? (int)pack_index(k) : 0;
       float acc[8];
       unpack8<DT>(lds_v4(st + (size_t)pkc * 16), acc);
 #pragma unroll
@@ -199,28 +197,38 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
         for (int e = 0; e < 8; ++e) ss = fmaf(zf[k][e], zf[k][e], ss);
       }
     }
-    float tot = 0.0f;
-    bool failed;
-    if (!p.skip_norm)
-      tot = block_allreduce<false>(ss, red_ss[i & 1], !ok, &failed);
-    else
-      failed = __syncthreads_or(!ok) != 0;
-    if (failed) {
-      if (threadIdx.x == 0) atomicExch(sp.err, 1);
-      // let this CTA's own copies still in flight land before shared memory is released
-      for (int64_t j = i; j < my_rows && j < i + S; ++j)
-        (void)mbar_wait_bounded(&full_bar[j % S], (uint32_t)((j / S) & 1), sp.wait_cycles);
-      return;
+    return ok;
+  };
+
+  // After a failed wait on row i (stage s, phase parity): record the error and let this
+  // CTA's own copies still in flight (rows i .. i+S-1) land before shared memory is released.
+  auto fail_out = [&](int64_t i, int s, uint32_t parity) {
+    if (threadIdx.x == 0) atomicExch(sp.err, 1);
+    for (int64_t j = i; j < my_rows && j < i + S; ++j) {
+      (void)mbar_wait_bounded(&full_bar[s], parity, sp.wait_cycles);
+      if (++s == S) {
+        s = 0;
+        parity ^= 1u;
+      }
     }
-    // every thread has read stage s: refill it with the row S iterations ahead
+  };
+
+  // Every thread has read row i's stage s: refill it with the row S iterations ahead.
+  auto refill_after = [&](int64_t i, int s) {
     if (threadIdx.x == 0 && i + S < my_rows) {
       fence_proxy_async_smem();
-      issue(s, first + (i + S) * stride);
+      issue(s, row_of(i + S));
     }
+  };
+
+  // residual_out and the normalised row: stores z and y (16-bit or fp32); with FP8 leaves
+  // the ROUNDED y in zf and returns this thread's part of its amax.
+  auto normalise_row = [&](int64_t i, const uint4 (&z)[PPT], float (&zf)[PPT][8], float tot) -> float {
+    const int64_t row_e = out_base(i);
     if (p.res_out != nullptr) {
 #pragma unroll
       for (int k = 0; k < PPT; ++k)
-        if (valid[k]) st_v4(static_cast<uint16_t*>(p.res_out) + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8, z[k]);
+        if (valid[k]) st_v4(static_cast<uint16_t*>(p.res_out) + row_e + pack_index(k) * 8, z[k]);
     }
     const float inv = p.skip_norm ? 1.0f : rsqrtf(tot * p.inv_h + p.eps);
     uint4 y[PPT];
@@ -232,7 +240,7 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
       for (int e = 0; e < 8; ++e) yf[e] = (zf[k][e] * inv) * wv[k][e];
       y[k] = pack8<DT>(yf);
       if (p.out_f32 && valid[k]) {
-        float* o = static_cast<float*>(p.out) + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8;
+        float* o = static_cast<float*>(p.out) + row_e + pack_index(k) * 8;
         st_v4(o, make_uint4(__float_as_uint(yf[0]), __float_as_uint(yf[1]), __float_as_uint(yf[2]),
                             __float_as_uint(yf[3])));
         st_v4(o + 4, make_uint4(__float_as_uint(yf[4]), __float_as_uint(yf[5]), __float_as_uint(yf[6]),
@@ -249,33 +257,66 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
     if (p.out != nullptr && !p.out_f32) {
 #pragma unroll
       for (int k = 0; k < PPT; ++k)
-        if (valid[k]) st_v4(static_cast<uint16_t*>(p.out) + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8, y[k]);
+        if (valid[k]) st_v4(static_cast<uint16_t*>(p.out) + row_e + pack_index(k) * 8, y[k]);
     }
-    if (QUANT && p.group_lanes) {  // per group: lanes of a group combine, no block reduction
+    return amax;
+  };
+
+  // Per-token FP8 codes of row i from its rounded y and the row's amax.
+  auto quantise_row = [&](int64_t i, const float (&yq)[PPT][8], float am) {
+    const int64_t row_e = out_base(i);
+    const float scale = __fdiv_rn(am, 448.0f);
+    if (threadIdx.x == 0) st_f32(p.scale + row_of(i), scale);
+    const float rcp = am == 0.0f ? 0.0f : __frcp_rn(scale);
 #pragma unroll
-      for (int k = 0; k < PPT; ++k) {
-        const int pk = (int)threadIdx.x + k * (int)blockDim.x;
-        const uint2 cw = quant_pack_per_group(zf[k], p.group_lanes, valid[k],
-                                              p.scale + row * (int64_t)p.ngroups + pk / p.group_lanes);
-        if (valid[k]) st_v2(p.q + row_e + (int64_t)pk * 8, cw);
+    for (int k = 0; k < PPT; ++k) {
+      if (!valid[k]) continue;
+      uint32_t c[4] = {0u, 0u, 0u, 0u};  // an all-zero row keeps codes 0 (no division)
+      if (am != 0.0f) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          c[e] = e4m3x2(div_rn_by(yq[k][2 * e], scale, rcp), div_rn_by(yq[k][2 * e + 1], scale, rcp));
       }
-    } else if constexpr (QUANT) {
-      const float am = block_allreduce<true>(amax, red_amax[i & 1]);
-      const float scale = __fdiv_rn(am, 448.0f);
-      if (threadIdx.x == 0) st_f32(p.scale + row, scale);
-      const float rcp = am == 0.0f ? 0.0f : __frcp_rn(scale);
+      st_v2(p.q + row_e + pack_index(k) * 8, make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16)));
+    }
+  };
+
+  // stage and phase of row i, kept incrementally (i % S and i / S would be 64-bit divisions)
+  int s = 0;
+  uint32_t parity = 0;
+  for (int64_t i = 0; i < my_rows; ++i) {
+    uint4 z[PPT];
+    float zf[PPT][8], ss;
+    const bool ok = read_row(s, parity, z, zf, ss);
+    float tot = 0.0f;
+    bool failed;
+    if (!p.skip_norm)
+      tot = block_allreduce<false>(ss, red_ss[i & 1], !ok, &failed);
+    else
+      failed = __syncthreads_or(!ok) != 0;
+    if (failed) {
+      fail_out(i, s, parity);
+      return;
+    }
+    refill_after(i, s);
+    const float amax = normalise_row(i, z, zf, tot);
+    if constexpr (QUANT) {
+      if (p.group_lanes) {  // per group: lanes of a group combine, no block reduction
+        const int64_t row_e = out_base(i);
 #pragma unroll
-      for (int k = 0; k < PPT; ++k) {
-        if (!valid[k]) continue;
-        uint32_t c[4] = {0u, 0u, 0u, 0u};  // an all-zero row keeps codes 0 (no division)
-        if (am != 0.0f) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            c[e] = e4m3x2(div_rn_by(zf[k][2 * e], scale, rcp), div_rn_by(zf[k][2 * e + 1], scale, rcp));
+        for (int k = 0; k < PPT; ++k) {
+          const int pk = (int)threadIdx.x + k * (int)blockDim.x;
+          const uint2 cw = quant_pack_per_group(zf[k], p.group_lanes, valid[k],
+                                                p.scale + row_of(i) * (int64_t)p.ngroups + pk / p.group_lanes);
+          if (valid[k]) st_v2(p.q + row_e + (int64_t)pk * 8, cw);
         }
-        st_v2(p.q + row_e + (int64_t)((int)threadIdx.x + k * (int)blockDim.x) * 8,
-              make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16)));
+      } else {  // per token: the row's amax over the block
+        quantise_row(i, zf, block_allreduce<true>(amax, red_amax[i & 1]));
       }
+    }
+    if (++s == S) {
+      s = 0;
+      parity ^= 1u;
     }
   }
 }
