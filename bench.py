@@ -290,40 +290,28 @@ def time_graph(sets, ctx, calls: int, steps: int, warmup: int, world: int, sampl
     return elapsed_ms, t0, t1, step_ms
 
 
-def e2e_fused(ctx, wl, steps: int, dev):
-    """Same metric end to end: pinned host inputs -> device, the fused call, outputs -> pinned host."""
+def _host_buffers(wl):
+    """Pinned host inputs and outputs of one call of the workload."""
     import torch
     from tensor_all_reduce_gb300 import synth
     inp = wl.inputs()
     t = synth.TORCH_DTYPES[wl.dtype]
     m, h = wl.m, wl.h
-    h_parts = [p.pin_memory() for p in inp["partials"]]
-    h_res = inp["residual"].pin_memory() if inp["residual"] is not None else None
-    h_w = inp["weight"].pin_memory()
-    d_parts = [torch.empty((m, h), dtype=t, device=dev) for _ in range(wl.n)]
-    d_res = torch.empty((m, h), dtype=t, device=dev) if h_res is not None else None
-    d_w = torch.empty((h,), dtype=t, device=dev)
-    d_out = torch.empty((m, h), dtype=t, device=dev)
-    d_ro = torch.empty((m, h), dtype=t, device=dev) if h_res is not None else None
-    d_q = torch.empty((m, h), dtype=torch.uint8, device=dev) if wl.quant else None
-    d_sc = torch.empty((m,), dtype=torch.float32, device=dev) if wl.quant else None
-    outs_d = [x for x in (d_out, d_ro, d_q, d_sc) if x is not None]
-    outs_h = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs_d]
-    h2d = sum(x.numel() * x.element_size() for x in h_parts + [h_w] + ([h_res] if h_res is not None else []))
-    d2h = sum(x.numel() * x.element_size() for x in outs_d)
+    ins = {"partials": [p.pin_memory() for p in inp["partials"]],
+           "residual": inp["residual"].pin_memory() if inp["residual"] is not None else None,
+           "weight": None if wl.skip_norm else inp["weight"].pin_memory()}
+    outs = {"out": torch.empty((m, h), dtype=torch.float32 if wl.out_fp32 else t, pin_memory=True)
+            if (wl.mirror or not wl.quant) else None,
+            "residual_out": torch.empty((m, h), dtype=t, pin_memory=True) if wl.residual else None,
+            "q_out": torch.empty((m, h), dtype=torch.uint8, pin_memory=True) if wl.quant else None,
+            "scale_out": torch.empty((m, h // wl.group) if wl.group else (m,), dtype=torch.float32, pin_memory=True)
+            if wl.quant else None}
+    nbytes = lambda xs: sum(x.numel() * x.element_size() for x in xs if x is not None)
+    return ins, outs, nbytes(ins["partials"] + [ins["residual"], ins["weight"]]), nbytes(outs.values())
 
-    def step():
-        for d, hh in zip(d_parts, h_parts):
-            d.copy_(hh, non_blocking=True)
-        if d_res is not None:
-            d_res.copy_(h_res, non_blocking=True)
-        d_w.copy_(h_w, non_blocking=True)
-        ctx.fused_reduce_rmsnorm(d_parts, d_res, d_w, eps=1e-6, gemma=wl.gemma, quant=wl.quant, out=d_out,
-                                 residual_out=d_ro, q_out=d_q, scale_out=d_sc,
-                                 want_residual_out=d_ro is not None)
-        for hh, d in zip(outs_h, outs_d):
-            hh.copy_(d, non_blocking=True)
 
+def _time_steps(step, steps: int):
+    import torch
     for _ in range(2):
         step()
     torch.cuda.synchronize()
@@ -333,7 +321,53 @@ def e2e_fused(ctx, wl, steps: int, dev):
         step()
     end.record()
     end.synchronize()
-    return start.elapsed_time(end) * 1000.0 / steps, h2d, d2h
+    return start.elapsed_time(end) * 1000.0 / steps
+
+
+def e2e_fused(ctx, wl, steps: int, dev):
+    """Same metric end to end through the C-ABI call on HOST buffers (ar_fused_reduce_rmsnorm_host):
+    the inputs sit in pinned host memory, the kernel reads them across the CPU-GPU link and
+    writes every output into pinned host memory, so each step's whole host->device and
+    device->host traffic is inside the timed region.  Returns (us per call, bytes in, bytes out)."""
+    import torch
+    import tensor_all_reduce_gb300 as tar
+    from tensor_all_reduce_gb300 import synth
+    ins, outs, h2d, d2h = _host_buffers(wl)
+    ptr = lambda x: None if x is None else x.data_ptr()
+    code = {"bf16": tar.AR_DTYPE_BF16, "fp16": tar.AR_DTYPE_F16}[wl.dtype]
+    args = tar.make_fused_args([p.data_ptr() for p in ins["partials"]], ptr(ins["residual"]),
+                               ptr(outs["residual_out"]), ptr(ins["weight"]), ptr(outs["out"]), 1e-6, wl.gemma,
+                               wl.quant, ptr(outs["q_out"]), ptr(outs["scale_out"]), wl.m, wl.h, code,
+                               skip_norm=wl.skip_norm, out_fp32=wl.out_fp32, group_size=wl.group)
+    stream = torch.cuda.current_stream().cuda_stream
+    us = _time_steps(lambda: tar.ar_fused_reduce_rmsnorm_host(ctx.handle, args, stream), steps)
+    return us, h2d, d2h
+
+
+def e2e_copy_engines(ctx, wl, steps: int, dev):
+    """The same call with explicit copies instead: pinned host inputs copied to device buffers,
+    the device-memory call, the outputs copied back (for comparison with e2e_fused)."""
+    import torch
+    ins, outs, _, _ = _host_buffers(wl)
+    d_ins = {k: (None if v is None else [p.to(dev) for p in v] if k == "partials" else v.to(dev))
+             for k, v in ins.items()}
+    d_outs = {k: (None if v is None else torch.empty(v.shape, dtype=v.dtype, device=dev)) for k, v in outs.items()}
+
+    def step():
+        for d, hh in zip(d_ins["partials"], ins["partials"]):
+            d.copy_(hh, non_blocking=True)
+        for k in ("residual", "weight"):
+            if ins[k] is not None:
+                d_ins[k].copy_(ins[k], non_blocking=True)
+        ctx.fused_reduce_rmsnorm(d_ins["partials"], d_ins["residual"], d_ins["weight"], eps=1e-6, gemma=wl.gemma,
+                                 quant=wl.quant, want_out=wl.mirror or not wl.quant, want_residual_out=wl.residual,
+                                 skip_norm=wl.skip_norm,
+                                 out_fp32=wl.out_fp32, group_size=wl.group, **d_outs)
+        for k, hh in outs.items():
+            if hh is not None:
+                hh.copy_(d_outs[k], non_blocking=True)
+
+    return _time_steps(step, steps)
 
 
 # ---------------------------------------------------------------------------
@@ -535,6 +569,7 @@ def main(argv=None):
 
     e2e_us, h2d, d2h = e2e_fused(ctx, wl, args.e2e_steps, dev)
     e2e_us = max_over_ranks(e2e_us, world, dev) / world
+    copy_us = e2e_copy_engines(ctx, wl, args.e2e_steps, dev)
 
     extra = {}
     if rank == 0 and not args.no_sweep:
@@ -557,7 +592,10 @@ def main(argv=None):
                          "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name),
                          "peak_kind": peak_kind, "algorithmic_bytes_per_launch": fp},
             "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "note": "one call per step: inputs copied from pinned host memory, outputs copied back"},
+                    "api": "ar_fused_reduce_rmsnorm_host",
+                    "note": "one C-ABI call per step on pinned host buffers: the kernel reads the inputs from and "
+                            "writes the outputs to host memory across the CPU-GPU link",
+                    "copy_engines_us": round(copy_us, 3)},
             "per_step": {"median": round(statistics.median(step_ms) * 1000.0 / calls, 3),
                          "min": round(min(step_ms) * 1000.0 / calls, 3),
                          "max": round(max(step_ms) * 1000.0 / calls, 3), "unit": UNIT,

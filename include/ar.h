@@ -191,6 +191,29 @@ ar_status ar_device_status(ar_ctx* ctx, int* code);
 ar_status ar_fused_reduce_rmsnorm_batch(ar_ctx* ctx, const ar_fused_args* calls, int count, void* stream);
 
 /*
+ * ar_fused_reduce_rmsnorm over buffers in host memory: the same operation, arguments and
+ * error rules, where any buffer (partials, residual_in/out, weight, out, q_out, scale_out)
+ * may instead be page-locked host memory (cudaHostAlloc / cudaMallocHost, or
+ * cudaHostRegister'ed) that the device can address.  The kernel reads the inputs from, and
+ * writes the results into, that memory directly across the CPU-GPU link (on GB300 the
+ * NVLink-C2C link to the Grace CPU), so the host<->device transfer and the computation are
+ * one pass with no device staging buffers.  There is no counterpart on the pages; it is the
+ * end-to-end form of the call for data that lives on the host.
+ *
+ * Each pointer is looked up with cudaPointerGetAttributes: page-locked host memory is
+ * replaced by its device address, device memory of the context's device is used as is,
+ * and anything else (pageable host memory, another device's memory) returns
+ * AR_ERR_INVALID_ARG without launching (ar_last_error says why).  Only the kernels that
+ * reach memory through plain loads and stores run (the one-CTA-per-row and cluster
+ * forms); AR_OPT_FORCE_VARIANT = 3 (staged) returns AR_ERR_UNSUPPORTED here.
+ *
+ * Asynchronous like the device form: the results are in host memory once `stream` has
+ * been synchronised, and the host must not write the inputs or read the outputs before.
+ * Nothing is allocated; the call can be captured in a CUDA graph.
+ */
+ar_status ar_fused_reduce_rmsnorm_host(ar_ctx* ctx, const ar_fused_args* args, void* stream);
+
+/*
  * Allocation-free form of ar_fused_reduce_rmsnorm, for callers that cannot call
  * cudaMalloc where they need this op: an engine that has handed all device memory to a
  * fixed plan (weights, KV cache, activations) up front, code running inside a stream

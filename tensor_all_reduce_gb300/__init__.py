@@ -99,6 +99,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ar_destroy.argtypes = [vp]
     lib.ar_reduce_sum.argtypes = [vp, vp, ctypes.POINTER(vp), c_int, i64, c_int, vp]
     lib.ar_fused_reduce_rmsnorm.argtypes = [vp, ctypes.POINTER(ArFusedArgs), vp]
+    lib.ar_fused_reduce_rmsnorm_host.argtypes = [vp, ctypes.POINTER(ArFusedArgs), vp]
     lib.ar_status_string.argtypes = [c_int]
     lib.ar_status_string.restype = ctypes.c_char_p
     lib.ar_last_error.argtypes = [vp]
@@ -110,7 +111,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ar_device_status.argtypes = [vp, ctypes.POINTER(c_int)]
     lib.ar_fused_reduce_rmsnorm_batch.argtypes = [vp, ctypes.POINTER(ArFusedArgs), c_int, vp]
     for f in ("ar_init", "ar_destroy", "ar_reduce_sum", "ar_fused_reduce_rmsnorm", "ar_set_option",
-              "ar_get_info", "ar_device_status", "ar_fused_reduce_rmsnorm_batch"):
+              "ar_get_info", "ar_device_status", "ar_fused_reduce_rmsnorm_batch", "ar_fused_reduce_rmsnorm_host"):
         getattr(lib, f).restype = c_int
     _lib = lib
     return lib
@@ -193,6 +194,14 @@ def ar_fused_reduce_rmsnorm(ctx: int, args: ArFusedArgs, stream: Optional[int] =
     return st
 
 
+def ar_fused_reduce_rmsnorm_host(ctx: int, args: ArFusedArgs, stream: Optional[int] = None,
+                                 raise_on_error: bool = True) -> int:
+    st = load_library().ar_fused_reduce_rmsnorm_host(ctx, ctypes.byref(args), stream)
+    if raise_on_error:
+        _check(ctx, st, "ar_fused_reduce_rmsnorm_host")
+    return st
+
+
 def ar_fused_reduce_rmsnorm_batch(ctx: int, calls: Sequence[ArFusedArgs], stream: Optional[int] = None,
                                   raise_on_error: bool = True) -> int:
     arr = (ArFusedArgs * max(len(calls), 1))(*calls)
@@ -249,15 +258,18 @@ def _stream(stream) -> int:
     return stream.cuda_stream
 
 
-def _row_stride(tensors, m, h, dtype, what) -> int:
-    """The common row stride (in elements) of [m, h] CUDA tensors with unit column stride."""
+def _row_stride(tensors, m, h, dtype, what, host: bool = False) -> int:
+    """The common row stride (in elements) of [m, h] CUDA tensors (with `host`, CUDA or
+    pinned host tensors) with unit column stride."""
     ld = None
     for t in tensors:
         if t is None:
             continue
-        if t.shape != (m, h) or not t.is_cuda or (dtype is not None and t.dtype != dtype) or \
+        placed = t.is_cuda or (host and t.is_pinned())
+        if t.shape != (m, h) or not placed or (dtype is not None and t.dtype != dtype) or \
                 (h > 1 and t.stride(1) != 1) or (m > 1 and t.stride(0) < h):
-            raise ValueError(f"{what} must be [m, h] CUDA tensors with unit column stride")
+            kind = "CUDA or pinned host" if host else "CUDA"
+            raise ValueError(f"{what} must be [m, h] {kind} tensors with unit column stride")
         s = t.stride(0) if m > 1 else h
         if ld is not None and s != ld:
             raise ValueError(f"{what} must share one row stride")
@@ -323,30 +335,50 @@ class Context:
         skip_norm there is no RMSNorm (weight may be None); with out_fp32 `out` is float32.
         Inputs (and given outputs) may have padded rows: unit column stride, one row stride
         for the inputs and one for the outputs; allocated outputs are contiguous."""
+        return self._fused(False, partials, residual, weight, eps, gemma, quant, out, residual_out, q_out,
+                           scale_out, want_out, want_residual_out, stream, skip_norm, out_fp32, group_size)
+
+    def fused_reduce_rmsnorm_host(self, partials, residual, weight, eps: float = 1e-6, gemma: bool = False,
+                                  quant: bool = False, out=None, residual_out=None, q_out=None, scale_out=None,
+                                  want_out: bool = True, want_residual_out: bool = True, stream=None,
+                                  skip_norm: bool = False, out_fp32: bool = False, group_size: int = 0):
+        """fused_reduce_rmsnorm where tensors may be pinned host tensors (or CUDA tensors of
+        this device): the kernel reads and writes host memory directly.  Outputs it allocates
+        are pinned host tensors.  Asynchronous: synchronise `stream` before reading them."""
+        return self._fused(True, partials, residual, weight, eps, gemma, quant, out, residual_out, q_out,
+                           scale_out, want_out, want_residual_out, stream, skip_norm, out_fp32, group_size)
+
+    def _fused(self, host, partials, residual, weight, eps, gemma, quant, out, residual_out, q_out, scale_out,
+               want_out, want_residual_out, stream, skip_norm, out_fp32, group_size):
         import torch
         x0 = partials[0]
         m, h = x0.shape
-        ld_in = _row_stride([*partials, residual], m, h, x0.dtype, "partials and residual")
+
+        def alloc(shape, dtype):
+            if host:
+                return torch.empty(shape, dtype=dtype, pin_memory=True)
+            return torch.empty(shape, dtype=dtype, device=x0.device)
+
+        ld_in = _row_stride([*partials, residual], m, h, x0.dtype, "partials and residual", host)
         given = [t for t in (out, residual_out, q_out) if t is not None]
-        ld_out = _row_stride(given, m, h, None, "outputs") if given else h
+        ld_out = _row_stride(given, m, h, None, "outputs", host) if given else h
         if ld_out != h and ((out is None and (want_out or not quant)) or (residual_out is None and want_residual_out)
                             or (quant and q_out is None)):
             raise ValueError("with padded outputs every output must be given")
         if out is None and (want_out or not quant):
-            out = torch.empty((m, h), dtype=torch.float32 if out_fp32 else x0.dtype, device=x0.device)
+            out = alloc((m, h), torch.float32 if out_fp32 else x0.dtype)
         if residual_out is None and want_residual_out:
-            residual_out = torch.empty((m, h), dtype=x0.dtype, device=x0.device)
+            residual_out = alloc((m, h), x0.dtype)
         if quant:
             if q_out is None:
-                q_out = torch.empty((m, h), dtype=torch.uint8, device=x0.device)
+                q_out = alloc((m, h), torch.uint8)
             if scale_out is None:
-                shape = (m, h // group_size) if group_size else (m,)
-                scale_out = torch.empty(shape, dtype=torch.float32, device=x0.device)
+                scale_out = alloc((m, h // group_size) if group_size else (m,), torch.float32)
         args = make_fused_args([p.data_ptr() for p in partials], _ptr(residual), _ptr(residual_out),
                                _ptr(weight), _ptr(out), eps, gemma, quant, _ptr(q_out), _ptr(scale_out),
                                m, h, _torch_dtype_code(x0), skip_norm=skip_norm, out_fp32=out_fp32,
                                group_size=group_size, ld_in=ld_in, ld_out=ld_out)
-        ar_fused_reduce_rmsnorm(self.handle, args, _stream(stream))
+        (ar_fused_reduce_rmsnorm_host if host else ar_fused_reduce_rmsnorm)(self.handle, args, _stream(stream))
         return out, residual_out, q_out, scale_out
 
     def fused_reduce_rmsnorm_batch(self, calls, stream=None):

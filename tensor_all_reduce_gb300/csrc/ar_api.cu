@@ -395,7 +395,10 @@ ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int
 // fused reduce + residual + RMSNorm (+ FP8)
 // ---------------------------------------------------------------------------
 
-ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* stream) {
+// The fused call.  `host`: some buffers are page-locked host memory (already resolved to
+// their device addresses), so only kernels that reach memory through plain loads and
+// stores run (bulk asynchronous copies are used on device memory only).
+static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, bool host) {
   if (!a) return AR_ERR_INVALID_ARG;
   if (a->n < 1 || a->n > AR_MAX_PARTIALS || a->m < 0 || a->h < 1 || (!a->weight && !a->skip_norm))
     return AR_ERR_INVALID_ARG;
@@ -491,7 +494,8 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   // kernel.
   const bool staged_auto = ctx->force_variant == 0 && ctx->cluster_size == 0 && ctx->ppt == 0 &&
                            (a->m < ctx->sm_count || a->m >= 4LL * ctx->sm_count);
-  if (ctx->force_variant == 3 || (staged_auto && staged_ok)) {
+  if (host && ctx->force_variant == 3) return AR_ERR_UNSUPPORTED;
+  if (!host && (ctx->force_variant == 3 || (staged_auto && staged_ok))) {
     if (!staged_ok) return AR_ERR_UNSUPPORTED;
     // packs per thread: 1 (768 threads for h = 6144) when each CTA runs through many rows
     // with the norm and at most 4 partials, else 2 (same A/B runs: 1 pack was ~1 % faster on
@@ -569,7 +573,9 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
   const int chunk = (row_packs + csize - 1) / csize;
   if (chunk > kMaxPacksPerCta) return AR_ERR_UNSUPPORTED;  // h > 8192 * max cluster size
   int ppt = vec ? ctx->ppt : 1;
-  if (ppt == 0) ppt = chunk <= 256 ? 1 : 2;
+  // one pack per thread for short rows, and over host memory (the most loads in flight
+  // per SM: measured fastest across the C2C link), else two
+  if (ppt == 0) ppt = (chunk <= 256 || host) ? 1 : 2;
   int block = ((chunk + ppt - 1) / ppt + 31) / 32 * 32;
   if (block < 32) block = 32;
   const int64_t grid = a->m * csize;
@@ -612,6 +618,57 @@ ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* str
       ctx->last_variant = csize > 1 ? "fused_cluster_scalar" : "fused_scalar";
   }
   return st;
+}
+
+ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* a, void* stream) {
+  return fused_impl(ctx, a, stream, false);
+}
+
+// Device address of a buffer that is device memory of the context's device or page-locked
+// host memory mapped into the device's address space; anything else is refused.
+static ar_status resolve_buffer(const ar_ctx* ctx, const void* p, const void** out) {
+  *out = nullptr;
+  if (!p) return AR_OK;
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return AR_ERR_INVALID_ARG;
+  }
+  if (at.type == cudaMemoryTypeHost) {
+    if (!at.devicePointer) return AR_ERR_INVALID_ARG;
+    *out = at.devicePointer;
+    return AR_OK;
+  }
+  if (at.type == cudaMemoryTypeDevice && at.device == ctx->device) {
+    *out = p;
+    return AR_OK;
+  }
+  return AR_ERR_INVALID_ARG;  // pageable host memory, or another device's memory
+}
+
+ar_status ar_fused_reduce_rmsnorm_host(ar_ctx* ctx, const ar_fused_args* a, void* stream) {
+  // the argument rules of the device entry (they compare addresses only)
+  const ar_status v = fused_impl(nullptr, a, nullptr, true);
+  if (v != AR_ERR_NOT_INITIALIZED) return v;
+  if (!ctx) return AR_ERR_NOT_INITIALIZED;
+  DeviceGuard g(ctx->device);
+  ar_fused_args d = *a;
+  ar_status st = AR_OK;
+  for (int r = 0; r < a->n && st == AR_OK; ++r) st = resolve_buffer(ctx, a->partials[r], &d.partials[r]);
+  const void* t = nullptr;
+  if (st == AR_OK) st = resolve_buffer(ctx, a->residual_in, &d.residual_in);
+  if (st == AR_OK && (st = resolve_buffer(ctx, a->residual_out, &t)) == AR_OK) d.residual_out = const_cast<void*>(t);
+  if (st == AR_OK) st = resolve_buffer(ctx, a->weight, &d.weight);
+  if (st == AR_OK && (st = resolve_buffer(ctx, a->out, &t)) == AR_OK) d.out = const_cast<void*>(t);
+  if (st == AR_OK && (st = resolve_buffer(ctx, a->q_out, &t)) == AR_OK) d.q_out = const_cast<void*>(t);
+  if (st == AR_OK && (st = resolve_buffer(ctx, a->scale_out, &t)) == AR_OK)
+    d.scale_out = static_cast<float*>(const_cast<void*>(t));
+  if (st != AR_OK) {
+    snprintf(ctx->last_error, sizeof(ctx->last_error),
+             "a buffer is neither device memory of this device nor page-locked host memory");
+    return st;
+  }
+  return fused_impl(ctx, &d, stream, true);
 }
 
 // ---------------------------------------------------------------------------

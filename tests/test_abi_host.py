@@ -84,7 +84,7 @@ def test_reduce_validation(lib):
     assert reduce_status(out, p, 0) == tar.AR_ERR_NOT_INITIALIZED              # empty is valid
 
 
-def fused(**kw):
+def fused_args(**kw):
     m, h = kw.pop("m", 16), kw.pop("h", 6144)
     tb = m * h * 2
     d = dict(partials=[BASE + i * 64 * MB for i in range(4)], residual_in=BASE + 4 * 64 * MB,
@@ -97,7 +97,11 @@ def fused(**kw):
     a = tar.make_fused_args(**d)
     if n_override is not None:
         a.n = n_override
-    return tar.ar_fused_reduce_rmsnorm(None, a, None, raise_on_error=False)
+    return a
+
+
+def fused(**kw):
+    return tar.ar_fused_reduce_rmsnorm(None, fused_args(**kw), None, raise_on_error=False)
 
 
 def test_fused_validation(lib):
@@ -190,3 +194,20 @@ def test_batch_validation(lib):
     assert st([call(BASE), call(B2, residual_out=BASE + 5 * 64 * MB)]) == OV   # same output
     assert st([call(BASE), call(B2, h=0)]) == IA                    # per-call rules apply
 
+
+
+def test_host_entry_validates_like_the_device_entry(lib):
+    # ar_fused_reduce_rmsnorm_host applies the device entry's argument rules before it looks
+    # at what memory the pointers name
+    QG = dict(quant=True, q_out=BASE + 8 * 64 * MB, scale_out=BASE + 9 * 64 * MB)
+    cases = [dict(), dict(m=0), dict(h=0), dict(m=-1), dict(weight=None), dict(weight=None, skip_norm=True),
+             dict(out=None), dict(dtype=tar.AR_DTYPE_F32), dict(eps=float("nan")), dict(n=9),
+             dict(out=BASE + 7 * 64 * MB + 1), dict(out=BASE + 32), dict(residual_out=BASE + 7 * 64 * MB),
+             dict(group_size=128, **QG), dict(group_size=100, **QG), dict(group_size=128, h=16384, m=4, **QG),
+             dict(ld_in=6000), dict(ld_in=6144 + 64, ld_out=6144 + 8), dict(out_fp32=True, out=BASE)]
+    for kw in cases:
+        a = fused_args(**dict(kw))
+        dev_st = tar.ar_fused_reduce_rmsnorm(None, a, None, raise_on_error=False)
+        host_st = tar.ar_fused_reduce_rmsnorm_host(None, a, None, raise_on_error=False)
+        assert host_st == dev_st, (kw, host_st, dev_st)
+    assert lib.ar_fused_reduce_rmsnorm_host(None, None, None) == tar.AR_ERR_INVALID_ARG
