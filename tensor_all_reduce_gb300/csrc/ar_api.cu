@@ -485,15 +485,19 @@ static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, b
   const int64_t stage_bytes = (int64_t)rows_per_stage * a->h * es;
   // Stages per CTA: two stages in one CTA per SM stream best with every epilogue (three
   // stages, or one stage and two CTAs per SM, were slower in same-GPU A/B runs on GB300 at
-  // N = 4 and 8, h = 6144 and 7168, m = 1024 .. 4096).
-  int S = ctx->stages ? ctx->stages : 2;
+  // N = 4 and 8, h = 6144 and 7168, m = 1024 .. 4096).  With one to two rows per SM a
+  // single stage lets every row have its own resident CTA.
+  const bool one_row_per_cta = a->m >= ctx->sm_count && a->m <= 2LL * ctx->sm_count;
+  int S = ctx->stages ? ctx->stages : (one_row_per_cta ? 1 : 2);
   if (!ctx->stages && S * stage_bytes > ctx->max_dyn_smem) S = 1;
   const bool staged_ok = vec && row_packs <= 1024 && S * stage_bytes <= ctx->max_dyn_smem;
-  // Automatic choice: fewer rows than SMs -> one staged CTA per row (bulk row loads have
-  // the lowest latency); 1..4 rows per SM -> the row kernel; more -> the persistent staged
-  // kernel.
+  // Automatic choice (same-GPU sweeps on GB300, N = 4, h = 6144, m = 1 .. 512, with and
+  // without FP8): up to two rows per SM -> one staged CTA per row, all resident at once
+  // (bulk row loads have the lowest latency: 4.4 against 5.8 us for the row kernel at
+  // m = 152); 2..3 rows per SM -> the persistent staged kernel; 3..4 rows per SM -> the row
+  // kernel (every row's loads in flight at once); more -> the persistent staged kernel.
   const bool staged_auto = ctx->force_variant == 0 && ctx->cluster_size == 0 && ctx->ppt == 0 &&
-                           (a->m < ctx->sm_count || a->m >= 4LL * ctx->sm_count);
+                           (a->m < 3LL * ctx->sm_count || a->m >= 4LL * ctx->sm_count);
   if (host && ctx->force_variant == 3) return AR_ERR_UNSUPPORTED;
   if (!host && (ctx->force_variant == 3 || (staged_auto && staged_ok))) {
     if (!staged_ok) return AR_ERR_UNSUPPORTED;
