@@ -474,7 +474,7 @@ def sweep(ctx, dev, l2, peak):
     import torch
     from tensor_all_reduce_gb300 import synth
     out = []
-    for wl in synth.all_fused() + synth.options() + synth.reduce_only():
+    for wl in synth.all_fused() + synth.options() + synth.reduce_only() + synth.reduce_large():
         fused = isinstance(wl, synth.FusedWorkload)
         fp = wl.algorithmic_bytes()
         R = rotation_sets(fp, l2)

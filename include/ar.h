@@ -251,9 +251,11 @@ const char* ar_status_string(ar_status s);
 const char* ar_last_error(const ar_ctx* ctx);
 
 /* Name of the kernel variant the last successful call launched (tests assert on it):
- * "reduce_vec", "reduce_vec_tail", "reduce_scalar", "fused_row_vec", "fused_cluster_vec",
- * "fused_staged", "fused_scalar", "fused_cluster_scalar", "fused_batch",
- * "fused_batch_sequential" or "none" (empty call). */
+ * "reduce_vec", "reduce_vec_tail", "reduce_scalar", "reduce_staged" (a large 16-bit sum of
+ * 4-6 partials run by the staged fused kernel on the array viewed as rows, without residual
+ * or norm), "reduce_rows", "fused_row_vec", "fused_cluster_vec", "fused_staged",
+ * "fused_scalar", "fused_cluster_scalar", "fused_batch", "fused_batch_sequential" or "none"
+ * (empty call). */
 const char* ar_last_variant(const ar_ctx* ctx);
 
 /* Tuning and test overrides (0 = automatic for each, except AR_OPT_PDL).  Values outside

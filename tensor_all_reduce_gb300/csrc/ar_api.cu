@@ -330,6 +330,13 @@ ar_status ar_get_info(const ar_ctx* ctx, ar_info key, int64_t* value) {
 // plain reduce
 // ---------------------------------------------------------------------------
 
+static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, bool host);
+
+// Smallest 16-bit array reduced through the staged kernel, in elements per SM: sixteen rows
+// of the longest row length per SM (with fewer rows per CTA its pipeline fill and drain
+// cost more than the bulk copies gain).
+constexpr int64_t kStagedReduceMinElemsPerSm = 8192LL * 16;
+
 ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int n, int64_t numel,
                         ar_dtype dtype, void* stream) {
   if (!partials || n < 1 || n > AR_MAX_PARTIALS || numel < 0 || !dtype_ok(dtype)) return AR_ERR_INVALID_ARG;
@@ -359,6 +366,37 @@ ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int
   for (int r = 0; r < n; ++r) vec = vec && aligned(partials[r], 16);
   if (ctx->force_variant == 4) vec = false;
 
+  // Large 16-bit arrays of 4 to 6 partials: the same sum through the staged fused kernel on
+  // the array viewed as rows (no residual, no norm; the rounded sum is stored as the output,
+  // bit for bit the value below).  Same-GPU A/B on GB300 at 25M elements: N = 4 at 95.7 %
+  // of the measured copy bandwidth against 88.0 % for the per-thread kernel, N = 6 99.1 %
+  // against 96.0 %; with fewer partials they tie, with eight the per-thread kernel wins.
+  if (es == 2 && vec && n >= 4 && n <= 6 && ctx->force_variant == 0 && ctx->reduce_unroll == 0 &&
+      numel >= kStagedReduceMinElemsPerSm * ctx->sm_count) {
+    // the longest row that divides the array and leaves room for two stages of N rows
+    int64_t h = 0;
+    for (int64_t c : {8192, 7168, 6144, 5120, 4096, 3072, 2048})
+      if (numel % c == 0 && 2 * n * c * es <= ctx->max_dyn_smem) {
+        h = c;
+        break;
+      }
+    if (h) {
+      ar_fused_args fa;
+      memset(&fa, 0, sizeof(fa));
+      fa.n = n;
+      for (int r = 0; r < n; ++r) fa.partials[r] = partials[r];
+      fa.out = out;
+      fa.m = numel / h;
+      fa.h = h;
+      fa.dtype = dtype;
+      fa.skip_norm = 1;
+      fa.quant = AR_QUANT_NONE;
+      const ar_status st = fused_impl(ctx, &fa, stream, false);
+      if (st == AR_OK) ctx->last_variant = strcmp(ctx->last_variant, "fused_staged") == 0 ? "reduce_staged" : "reduce_rows";
+      return st;
+    }
+  }
+
   DeviceGuard g(ctx->device);
   const int max_grid = ctx->sm_count * (2048 / kReduceBlock);
   unsigned grid;
@@ -367,8 +405,13 @@ ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int
   if (vec) {
     const int epp = 16 / es;
     p.npacks = numel / epp;
+    // Four packs per thread per tile for large arrays, except with 16-bit elements and six
+    // or more partials, where one pack streams far better (same-GPU sweep on GB300, 6M and
+    // 25M elements: bf16 N = 8 at 104 % of the measured copy bandwidth with one pack against
+    // 73 % with four, N = 6 97 % against 82 %; N <= 4 and fp32 gain 1-9 % from four).
     int unroll = ctx->reduce_unroll;
-    if (unroll == 0) unroll = (p.npacks >= (int64_t)max_grid * kReduceBlock * 4) ? 4 : 1;
+    if (unroll == 0)
+      unroll = (p.npacks >= (int64_t)max_grid * kReduceBlock * 4 && (es == 4 || n <= 4)) ? 4 : 1;
     const int64_t tile = (int64_t)kReduceBlock * unroll;
     p.full_tiles = p.npacks / tile;
     const bool has_tail = (p.npacks % tile) != 0 || (numel % epp) != 0;

@@ -129,6 +129,14 @@ def reduce_only() -> List[ReduceWorkload]:
     return out
 
 
+def reduce_large() -> List[ReduceWorkload]:
+    """Streaming sizes of the plain reduce (well above L2): 4 and 8 partials of 4096 x 6144
+    bf16 (48 MiB each), and 4 of the same shape in fp32."""
+    return [ReduceWorkload("reduce_n4_m4096_h6144_bf16", 4, 4096 * 6144, "bf16", seed=1238, shape=(4096, 6144)),
+            ReduceWorkload("reduce_n8_m4096_h6144_bf16", 8, 4096 * 6144, "bf16", seed=1238, shape=(4096, 6144)),
+            ReduceWorkload("reduce_n4_m4096_h6144_fp32", 4, 4096 * 6144, "fp32", seed=1238, shape=(4096, 6144))]
+
+
 def decode_sweep() -> List[FusedWorkload]:
     return [FusedWorkload(f"n4_m{m}_h6144_bf16_decode", 4, m, 6144, seed=1236) for m in (1, 16, 64, 256)]
 
@@ -157,7 +165,7 @@ def all_fused() -> List[FusedWorkload]:
 
 
 def by_name(name: str):
-    for w in all_fused() + options() + reduce_only():
+    for w in all_fused() + options() + reduce_only() + reduce_large():
         if w.name == name:
             return w
     raise KeyError(name)

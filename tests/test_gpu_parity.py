@@ -313,12 +313,40 @@ def run_reduce(ctx, dev, parts_cpu, dtype, out_offset=0, in_offset=0):
     return synth.bits(g_out.t.cpu()), ctx.last_variant
 
 
-@pytest.mark.parametrize("wl", synth.reduce_only(), ids=[w.name for w in synth.reduce_only()])
+REDUCE_WORKLOADS = synth.reduce_only() + synth.reduce_large()
+
+
+@pytest.mark.parametrize("wl", REDUCE_WORKLOADS, ids=[w.name for w in REDUCE_WORKLOADS])
 def test_reduce_workloads(ctx, dev, orc, wl):
     parts = synth.reduce_inputs(wl.n, wl.numel, wl.dtype, wl.seed)
     got, variant = run_reduce(ctx, dev, parts, wl.dtype)
     assert_bits_equal(got, orc.reduce_sum([synth.bits(p) for p in parts], wl.dtype), wl.name)
+    staged = wl.dtype != "fp32" and 4 <= wl.n <= 6 and wl.numel >= 8192 * 16 * ctx.info(tar.AR_INFO_SM_COUNT)
+    assert variant == "reduce_staged" if staged else variant.startswith("reduce_vec"), variant
+
+
+@pytest.mark.parametrize("n", [4, 5, 6])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_reduce_large_through_staged_rows(ctx, dev, orc, n, dtype):
+    """Large 16-bit arrays of 4-6 partials run on the staged kernel as rows (no residual, no
+    norm): the same bits as the oracle's rank-order fp32 sum, with guard regions intact, in
+    place too, and with row lengths other than 8192 (the array length picks the row)."""
+    for numel in (4096 * 6144, 7168 * 2999):            # rows of 8192, and of 7168
+        parts = synth.reduce_inputs(n, numel, dtype, seed=n + numel % 97)
+        ref = orc.reduce_sum([synth.bits(p) for p in parts], dtype)
+        got, variant = run_reduce(ctx, dev, parts, dtype)
+        assert variant == "reduce_staged", variant
+        assert_bits_equal(got, ref, f"{n} x {numel}")
+    d = to_dev(parts, dev)
+    ctx.reduce_sum(d, out=d[1])
+    torch.cuda.synchronize()
+    assert ctx.last_variant == "reduce_staged"
+    assert_bits_equal(synth.bits(d[1].cpu()), ref, "in place")
+    ctx.set_option(tar.AR_OPT_REDUCE_UNROLL, 1)            # the per-thread kernel agrees bit for bit
+    got, variant = run_reduce(ctx, dev, parts, dtype)
+    ctx.set_option(tar.AR_OPT_REDUCE_UNROLL, 0)
     assert variant.startswith("reduce_vec")
+    assert_bits_equal(got, ref, "per-thread kernel")
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16", "fp32"])
