@@ -426,16 +426,25 @@ def oracle_all_cores_us(wl, seconds: float = 4.0, runs: int = 3):
     return statistics.median(samples), cores, rows
 
 
-def cpu_baseline(wl, seconds: float = 12.0):
-    """Serial oracle (one thread), timed on a bounded sample of the workload's rows; beside it
-    the same oracle with the rows partitioned over all host cores."""
+def cpu_baseline(wl, seconds: float = 12.0, runs: int = 5):
+    """Serial oracle (one thread, pinned to one core), timed on a bounded sample of the
+    workload's rows; beside it the same oracle with the rows partitioned over all host cores."""
     us1, rows = oracle_sample_us(wl, 16)                 # size the sample
     per_row_s = us1 / 1e6 / wl.m
-    rows = max(16, min(wl.m, int(seconds / 3 / per_row_s)))
-    samples = [oracle_sample_us(wl, rows)[0] for _ in range(3)]
+    rows = max(16, min(wl.m, int(seconds / runs / per_row_s)))
+    pinned = hasattr(os, "sched_setaffinity")
+    if pinned:
+        cpus = os.sched_getaffinity(0)
+        os.sched_setaffinity(0, {min(cpus)})            # this thread only, restored below
+    try:
+        samples = [oracle_sample_us(wl, rows)[0] for _ in range(runs)]
+    finally:
+        if pinned:
+            os.sched_setaffinity(0, cpus)
     mt_us, cores, mt_rows = oracle_all_cores_us(wl)
     return {"value": statistics.median(samples), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"serial C oracle on {rows} of {wl.m} rows, median of 3 runs, scaled to a full call",
+            "sample": f"serial C oracle on {rows} of {wl.m} rows, one thread pinned to one core, median of "
+                      f"{runs} runs, scaled to a full call",
             "all_cores": {"value": round(mt_us, 3), "unit": UNIT, "cores": cores,
                           "sample": f"the same oracle, {mt_rows} of {wl.m} rows split in {cores} row blocks "
                                     f"over {cores} threads, median of 3 runs, scaled to a full call"}}
