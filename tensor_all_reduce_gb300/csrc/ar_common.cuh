@@ -243,16 +243,16 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+// Warp maximum of values that are all >= 0 (magnitudes): their binary32 bit patterns order
+// like the values, so one integer warp reduction gives the exact maximum in every lane.
+__device__ __forceinline__ float warp_max_magnitude(float v) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
 }
 
-// Block-wide sum (MAX=false) or max (MAX=true) returned to every thread: a butterfly in
-// each warp, one barrier, then a butterfly over the warp totals in every warp.  Both
-// partners of a butterfly step combine the same two operands, so every lane of every warp
-// ends with the same bits.  `buf` holds one float per warp and must not be reused by
+// Block-wide sum (MAX=false) or max of magnitudes (MAX=true, values >= 0) returned to every
+// thread: a warp reduction, one barrier, then a reduction over the warp totals in every
+// warp.  Both partners of a butterfly step combine the same two operands (and the integer
+// maximum is exact), so every lane of every warp ends with the same bits.  `buf` holds one float per warp and must not be reused by
 // another reduction before the next barrier.  When `any` is given, `flag` is OR-ed over the
 // block in the same barrier and the result stored there (a caller agrees on a failure at
 // no extra barrier).
@@ -260,7 +260,7 @@ template <bool MAX>
 __device__ __forceinline__ float block_allreduce(float v, float* buf, bool flag = false, bool* any = nullptr) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = (blockDim.x + 31) >> 5;
-  v = MAX ? warp_max(v) : warp_sum(v);
+  v = MAX ? warp_max_magnitude(v) : warp_sum(v);
   if (lane == 0) buf[warp] = v;
   if (any != nullptr)
     *any = __syncthreads_or(flag) != 0;
@@ -268,7 +268,7 @@ __device__ __forceinline__ float block_allreduce(float v, float* buf, bool flag 
     __syncthreads();
   // identity of the sum, and of the max of magnitudes (every caller's values are >= 0)
   const float t = lane < nwarps ? buf[lane] : 0.0f;
-  return MAX ? warp_max(t) : warp_sum(t);
+  return MAX ? warp_max_magnitude(t) : warp_sum(t);
 }
 
 // ---------------------------------------------------------------------------
@@ -305,7 +305,8 @@ __device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank) {
   return v;
 }
 
-// Combine one value per CTA over the cluster; every thread of every CTA gets the same
+// Combine one value per CTA over the cluster (a sum, or the max of values >= 0); every
+// thread of every CTA gets the same
 // result.  `slot` is this CTA's published value (written by thread 0 before the call),
 // `bcast` a one-float broadcast cell.  Starts with a full cluster barrier so every slot is
 // written and visible.  The caller must not let a CTA exit while a peer may still read
@@ -318,7 +319,7 @@ __device__ __forceinline__ float cluster_gather(const float* slot, float* bcast,
     const int lane = threadIdx.x;
     float v = 0.0f;  // identity for the sum, and for the max of magnitudes
     if (lane < csize) v = ld_dsmem(slot, (uint32_t)lane);
-    v = MAX ? warp_max(v) : warp_sum(v);
+    v = MAX ? warp_max_magnitude(v) : warp_sum(v);
     if (lane == 0) *bcast = v;
   }
   __syncthreads();
