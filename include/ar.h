@@ -254,6 +254,7 @@ const char* ar_last_error(const ar_ctx* ctx);
  * "reduce_vec", "reduce_vec_tail", "reduce_scalar", "reduce_staged" (a large 16-bit sum of
  * 4-6 partials run by the staged fused kernel on the array viewed as rows, without residual
  * or norm), "reduce_rows", "fused_row_vec", "fused_cluster_vec", "fused_staged",
+ * "fused_staged_cluster" (rows longer than 8192 elements split over a cluster of staged CTAs),
  * "fused_scalar", "fused_cluster_scalar", "fused_batch", "fused_batch_sequential" or "none"
  * (empty call). */
 const char* ar_last_variant(const ar_ctx* ctx);
@@ -262,9 +263,12 @@ const char* ar_last_variant(const ar_ctx* ctx);
  * the documented range return AR_ERR_INVALID_ARG. */
 typedef enum {
   AR_OPT_FORCE_VARIANT = 0,  /* 0 auto, 1 row, 2 cluster, 3 staged, 4 scalar (tail) */
-  AR_OPT_CLUSTER_SIZE = 1,   /* 0 auto, else 1, 2, 4, 8 or 16 CTAs per row */
-  AR_OPT_PACKS_PER_THREAD = 2, /* 0 auto, else 1, 2 or 4 16-byte packs per thread */
-  AR_OPT_REDUCE_UNROLL = 3,  /* 0 auto, else 1, 2 or 4 packs per thread per tile */
+  AR_OPT_CLUSTER_SIZE = 1,   /* 0 auto, else 1, 2, 4, 8 or 16 CTAs per row (with
+                                AR_OPT_FORCE_VARIANT = 3 and 2..8: the staged cluster form) */
+  AR_OPT_PACKS_PER_THREAD = 2, /* 0 auto, else 1, 2 or 4 16-byte packs per thread (1 or 2 in
+                                  the staged cluster form) */
+  AR_OPT_REDUCE_UNROLL = 3,  /* 0 auto, else 1 or 4 packs per thread per tile (a forced value
+                                also keeps large 16-bit sums off the staged kernel) */
   AR_OPT_STAGES = 4,         /* 0 auto, else 1..4 shared-memory stages per CTA (staged variant) */
   AR_OPT_PDL = 5,            /* 1 (the default): launch with programmatic dependent launch, so
                                 a kernel may be scheduled while its predecessor on the stream

@@ -127,6 +127,10 @@ int staged_kernel_list(const void** out, int cap) {
       for (int q = 0; q < 2; ++q) {
         const void* fn = dt ? batch_kernel_bf16(n, q != 0) : batch_kernel_f16(n, q != 0);
         if (fn && k < cap) out[k++] = fn;
+        for (int ppt = 1; ppt <= 2; ++ppt) {
+          fn = dt ? staged_cluster_kernel_bf16(n, ppt, q != 0) : staged_cluster_kernel_f16(n, ppt, q != 0);
+          if (fn && k < cap) out[k++] = fn;
+        }
       }
   return k;
 }
@@ -523,8 +527,125 @@ static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, b
   const int row_packs = (int)((a->h + 7) / 8);
   const int max_cl = ctx->max_cluster;
 
-  // ---- staged (bulk-copy pipelined, persistent) variant for large batches ----
+  // ---- staged (bulk-copy pipelined, persistent) variants ----
   const int rows_per_stage = a->n + (a->residual_in ? 1 : 0);
+  // kernel parameters of the staged forms: `chunk` packs of each row per CTA, `cl` CTAs per row
+  auto staged_params = [&](ar::FusedParams& p, ar::StagedParams& sp, int chunk, int cl, int stages) {
+    memset(&p, 0, sizeof(p));
+    for (int r = 0; r < a->n; ++r) p.x[r] = a->partials[r];
+    p.res_in = a->residual_in;
+    p.res_out = a->residual_out;
+    p.w = a->weight;
+    p.out = a->out;
+    p.q = static_cast<uint8_t*>(a->q_out);
+    p.scale = a->scale_out;
+    p.m = a->m;
+    p.h = (int)a->h;
+    p.row_packs = row_packs;
+    p.chunk_packs = chunk;
+    p.csize = cl;
+    p.eps = a->eps;
+    p.inv_h = (float)(1.0 / (double)a->h);
+    p.gemma = a->gemma != 0;
+    p.skip_norm = a->skip_norm != 0;
+    p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
+    p.group_lanes = per_group ? a->group_size / 8 : 0;
+    p.ngroups = per_group ? (int)(a->h / a->group_size) : 0;
+    p.ld_in = li;
+    p.ld_out = lo;
+    sp = ar::StagedParams{};
+    sp.stages = stages;
+    sp.row_bytes = chunk * 16;  // bytes of a row's chunk (a whole row without a cluster)
+    sp.err = ctx->d_status;
+    sp.wait_cycles = ctx->wait_cycles ? ctx->wait_cycles : 2000000000LL;  // about a second at 2 GHz
+    sp.stall_first = ctx->test_stall;
+  };
+
+  // Cluster form: rows longer than one CTA holds (more than 1024 packs) are split over 2 or
+  // 4 CTAs of a cluster, each staging its slice; forced with AR_OPT_FORCE_VARIANT = 3 and
+  // a cluster size.
+  if (!host && vec) {
+    DeviceGuard dg(ctx->device);
+    int cl = 0;
+    if (ctx->force_variant == 3 && ctx->cluster_size > 1) {
+      cl = ctx->cluster_size;
+    } else if (ctx->force_variant == 0 && ctx->cluster_size == 0 && ctx->ppt == 0 && row_packs > 1024) {
+      // 2 or 4 CTAs per row: of the sizes whose slices fit one CTA with two stages, the one
+      // that keeps the most threads resident per SM, then the smaller (same-GPU A/B on GB300:
+      // N = 4, h = 12288 at 90 % of the measured copy bandwidth with 4 CTAs, three per SM,
+      // against 88 % with 2; h = 16384 95 % with 2 against 90 % with 4; N = 8, h = 16384
+      // 96 % with 4; 8 CTAs per row was never faster where fewer fit, and is used only where
+      // they do not).  With few rows (at most a quarter as many as SMs) the larger size that
+      // fits, to engage more SMs (m = 16, h = 16384: 4.1 us with 4 CTAs, 4.8 with 2).
+      const bool few_rows = a->m * 4 <= ctx->sm_count;
+      int best = 0;
+      for (int c = 2; c <= 8; c *= 2) {
+        if (c == 8 && cl) break;
+        const int ch = row_packs / c;
+        const int64_t st2 = 2 * (int64_t)rows_per_stage * ch * 16;
+        if (row_packs % c || ch > 1024 || st2 > ctx->max_dyn_smem) continue;
+        const int thr = ((ch + 1) / 2 + 31) / 32 * 32;
+        const void* f = a->dtype == AR_DTYPE_BF16 ? ar::staged_cluster_kernel_bf16(a->n, 2, quant)
+                                                  : ar::staged_cluster_kernel_f16(a->n, 2, quant);
+        int per_sm = 1;
+        if (!f || cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, f, thr, (size_t)st2) != cudaSuccess) {
+          (void)cudaGetLastError();
+          per_sm = 1;
+        }
+        if (per_sm * thr > best || (few_rows && cl)) {
+          best = per_sm * thr;
+          cl = c;
+        }
+      }
+    }
+    if (cl > 1) {
+      const int chunk = row_packs / cl;
+      const int64_t cstage = (int64_t)rows_per_stage * chunk * 16;
+      int CS = ctx->stages ? ctx->stages : 2;
+      if (!ctx->stages && CS * cstage > ctx->max_dyn_smem) CS = 1;
+      // two packs per thread (one pack was 10-25 % slower in this form)
+      const int cppt = ctx->ppt ? ctx->ppt : 2;
+      const bool ok = cl <= 8 && row_packs % cl == 0 && chunk <= 1024 && (cppt == 1 || cppt == 2) &&
+                      CS * cstage <= ctx->max_dyn_smem && (!per_group || chunk % (a->group_size / 8) == 0);
+      if (ok) {
+        ar::FusedParams p;
+        ar::StagedParams sp;
+        staged_params(p, sp, chunk, cl, CS);
+        int block = ((chunk + cppt - 1) / cppt + 31) / 32 * 32;
+        if (block < 32) block = 32;
+        const void* fn = a->dtype == AR_DTYPE_BF16 ? ar::staged_cluster_kernel_bf16(a->n, cppt, quant)
+                                                   : ar::staged_cluster_kernel_f16(a->n, cppt, quant);
+        if (!fn) return AR_ERR_UNSUPPORTED;
+        DeviceGuard g(ctx->device);
+        // persistent grid: as many clusters as fit at once
+        cudaLaunchConfig_t oc = {};
+        oc.gridDim = dim3((unsigned)(cl * ctx->sm_count), 1, 1);
+        oc.blockDim = dim3((unsigned)block, 1, 1);
+        oc.dynamicSmemBytes = (size_t)(CS * cstage);
+        cudaLaunchAttribute at;
+        at.id = cudaLaunchAttributeClusterDimension;
+        at.val.clusterDim.x = (unsigned)cl;
+        at.val.clusterDim.y = 1;
+        at.val.clusterDim.z = 1;
+        oc.attrs = &at;
+        oc.numAttrs = 1;
+        int nclusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, fn, &oc) != cudaSuccess || nclusters < 1) {
+          (void)cudaGetLastError();
+          nclusters = ctx->sm_count / cl;
+        }
+        const int64_t clusters = a->m < nclusters ? a->m : nclusters;
+        void* args[2] = {&p, &sp};
+        ar_status st = launch(ctx, fn, (unsigned)(clusters * cl), (unsigned)block, cl, args, (size_t)(CS * cstage),
+                              stream);
+        if (st == AR_OK) ctx->last_variant = "fused_staged_cluster";
+        return st;
+      }
+      if (ctx->force_variant == 3) return AR_ERR_UNSUPPORTED;
+    }
+  }
+
+  // One CTA per row.
   const int64_t stage_bytes = (int64_t)rows_per_stage * a->h * es;
   // Stages per CTA: two stages in one CTA per SM stream best with every epilogue (three
   // stages, or one stage and two CTAs per SM, were slower in same-GPU A/B runs on GB300 at
@@ -554,34 +675,8 @@ static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, b
     int sblock = ((row_packs + sppt - 1) / sppt + 31) / 32 * 32;
     if (sblock < 32) sblock = 32;
     ar::FusedParams p;
-    memset(&p, 0, sizeof(p));
-    for (int r = 0; r < a->n; ++r) p.x[r] = a->partials[r];
-    p.res_in = a->residual_in;
-    p.res_out = a->residual_out;
-    p.w = a->weight;
-    p.out = a->out;
-    p.q = static_cast<uint8_t*>(a->q_out);
-    p.scale = a->scale_out;
-    p.m = a->m;
-    p.h = (int)a->h;
-    p.row_packs = row_packs;
-    p.chunk_packs = row_packs;
-    p.csize = 1;
-    p.eps = a->eps;
-    p.inv_h = (float)(1.0 / (double)a->h);
-    p.gemma = a->gemma != 0;
-    p.skip_norm = a->skip_norm != 0;
-    p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
-    p.group_lanes = per_group ? a->group_size / 8 : 0;
-    p.ngroups = per_group ? (int)(a->h / a->group_size) : 0;
-    p.ld_in = li;
-    p.ld_out = lo;
-    ar::StagedParams sp = {};
-    sp.stages = S;
-    sp.row_bytes = (int)(a->h * es);
-    sp.err = ctx->d_status;
-    sp.wait_cycles = ctx->wait_cycles ? ctx->wait_cycles : 2000000000LL;  // about a second at 2 GHz
-    sp.stall_first = ctx->test_stall;
+    ar::StagedParams sp;
+    staged_params(p, sp, row_packs, 1, S);
     const void* fn = a->dtype == AR_DTYPE_BF16 ? ar::staged_kernel_bf16(a->n, sppt, quant)
                                                : ar::staged_kernel_f16(a->n, sppt, quant);
     if (!fn) return AR_ERR_UNSUPPORTED;

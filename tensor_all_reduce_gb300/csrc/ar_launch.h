@@ -18,6 +18,11 @@ const void* fused_kernel_bf16(int n, int ppt, bool quant, bool vec);
 const void* staged_kernel_f16(int n, int ppt, bool quant);
 const void* staged_kernel_bf16(int n, int ppt, bool quant);
 
+// Cluster form of the staged kernel for rows longer than one CTA holds (a row split over
+// the CTAs of a cluster; ppt 1 or 2 packs per thread).
+const void* staged_cluster_kernel_f16(int n, int ppt, bool quant);
+const void* staged_cluster_kernel_bf16(int n, int ppt, bool quant);
+
 // Batched form of the staged kernel (2 packs per thread, one row per CTA).
 const void* batch_kernel_f16(int n, bool quant);
 const void* batch_kernel_bf16(int n, bool quant);

@@ -95,18 +95,79 @@ __device__ __forceinline__ uint4 lds_v4(const void* p) {
   return v;
 }
 
+// Address of `local` (this CTA's shared memory) in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t ra;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local)), "r"(rank));
+  return ra;
+}
+
+// Asynchronous stores into another CTA's shared memory that complete bytes on that CTA's
+// mbarrier (both addresses from cluster_addr).
+__device__ __forceinline__ void st_async_v2(uint32_t raddr, uint32_t a, uint32_t b, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(raddr),
+               "r"(a), "r"(b), "r"(rbar)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t raddr, uint32_t v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr), "r"(v),
+               "r"(rbar)
+               : "memory");
+}
+
+// Poll an mbarrier whose phase other CTAs of the cluster complete (acquire at cluster scope,
+// so their stores are visible after it) until the phase with `parity` completes or the cycle
+// budget runs out.
+__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, long long budget) {
+  const long long t0 = clock64();
+  for (;;) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (clock64() - t0 > budget) return false;
+  }
+}
+
 // The rows r = first + i * stride (i = 0, 1, ...) of one call, processed by this CTA
 // through its shared-memory ring.  Shared by the persistent kernel and the batched one.
 //
 // Per row there are one or two block reductions: the square-sum, and with per-token FP8
 // the amax of the rounded output.
-template <int DT, int N, int PPT, bool QUANT>
+//
+// CL (cluster form, for rows longer than one CTA holds): the p.csize (2..8) CTAs of a cluster share
+// each row, CTA rank r staging and processing packs [r * chunk, (r + 1) * chunk) of it
+// (chunk = p.chunk_packs; the rows split exactly).  After each block reduction, thread 0
+// sends the CTA's total to every peer with an asynchronous store into the peer's shared
+// memory that completes on the peer's receive mbarrier (no cluster-wide barrier per row);
+// every thread waits on its own CTA's receive barrier and adds the totals in rank order, so
+// the whole cluster holds the same bits.  The failure flag of the bounded waits travels with
+// the square-sum, so the CTAs of a cluster agree and leave together.  Receive buffers are
+// double-buffered by row parity: a peer can only send row i + 2's total after this CTA sent
+// row i + 1's, which it does after reading row i's.  Cluster barriers run only at the start
+// (receive barriers initialised before any peer sends) and at the end (no CTA exits while a
+// store to it may be in flight).
+template <int DT, int N, int PPT, bool QUANT, bool CL = false>
 __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedParams& sp, int64_t first,
                                             int64_t stride) {
   extern __shared__ __align__(128) uint8_t stage_mem[];
   __shared__ __align__(8) uint64_t full_bar[4];
   __shared__ float red_ss[2][32];
   __shared__ float red_amax[2][32];
+  // cluster form: receive barriers [square-sum, amax][row parity] and buffers [parity][rank]
+  __shared__ __align__(8) uint64_t rx_bar[2][2];
+  __shared__ __align__(8) uint32_t rx_ss[2][8][2];  // {square-sum bits, failure flag}
+  __shared__ __align__(8) uint32_t rx_am[2][8];
+
+  const int csize = CL ? p.csize : 1;
+  const int chunk = CL ? p.chunk_packs : p.row_packs;       // packs of a row this CTA handles
+  const int col0 = CL ? (int)cluster_ctarank() * chunk : 0;  // first of them
 
   const int S = sp.stages;
   const bool has_res = p.res_in != nullptr;
@@ -117,16 +178,23 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&full_bar[s], 1);
+    if (CL)
+      for (int k = 0; k < 2; ++k)
+        for (int b = 0; b < 2; ++b) mbar_init(&rx_bar[k][b], 1);
     mbar_fence_init();
   }
   __syncthreads();
+  if constexpr (CL) {  // every peer's receive barriers exist before anything is sent to them
+    cluster_arrive();
+    cluster_wait();
+  }
   pdl_wait_and_release();
 
   auto issue = [&](int s, int64_t row) {
     uint8_t* dst = stage_mem + (size_t)s * stage_bytes;
     mbar_arrive_expect_tx(&full_bar[s], stage_bytes);
     if (sp.stall_first && row == first) return;  // nothing will complete this phase
-    const size_t off = (size_t)row * (size_t)(p.ld_in ? p.ld_in : (int64_t)p.h) * 2;  // padded rows
+    const size_t off = (size_t)row * (size_t)(p.ld_in ? p.ld_in : (int64_t)p.h) * 2 + (size_t)col0 * 16;
 #pragma unroll
     for (int r = 0; r < N; ++r) bulk_g2s(dst + (size_t)r * row_bytes, (const uint8_t*)p.x[r] + off, row_bytes, &full_bar[s]);
     if (has_res) bulk_g2s(dst + (size_t)N * row_bytes, (const uint8_t*)p.res_in + off, row_bytes, &full_bar[s]);
@@ -144,13 +212,13 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
 #pragma unroll
   for (int k = 0; k < PPT; ++k) {
     const int pk = (int)threadIdx.x + k * (int)blockDim.x;
-    valid[k] = pk < p.row_packs;
+    valid[k] = pk < chunk;
     const int pkc = valid[k] ? pk : 0;
     if (p.skip_norm) {  // no norm: y = z * 1 * 1 = z exactly; the weight is not read
 #pragma unroll
       for (int e = 0; e < 8; ++e) wv[k][e] = 1.0f;
     } else {
-      unpack8<DT>(ld_keep(static_cast<const uint16_t*>(p.w) + (int64_t)pkc * 8), wv[k]);
+      unpack8<DT>(ld_keep(static_cast<const uint16_t*>(p.w) + (int64_t)(col0 + pkc) * 8), wv[k]);
       if (p.gemma) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) wv[k][e] = 1.0f + wv[k][e];
@@ -160,7 +228,8 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
 
   auto row_of = [&](int64_t i) { return first + i * stride; };
   auto out_base = [&](int64_t i) { return row_of(i) * (p.ld_out ? p.ld_out : (int64_t)p.h); };  // first output element
-  auto pack_index = [&](int k) { return (int64_t)((int)threadIdx.x + k * (int)blockDim.x); };
+  auto pack_index = [&](int k) { return (int64_t)((int)threadIdx.x + k * (int)blockDim.x); };  // in the chunk
+  auto gpack = [&](int k) { return (int64_t)col0 + pack_index(k); };                         // in the row
 
   // Wait for a row's stage s (bounded; `parity` selects the phase), then read it: rounded sum, residual add, this
   // thread's part of the square-sum.  A thread whose wait ran out still reads the stage
@@ -228,7 +297,7 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
     if (p.res_out != nullptr) {
 #pragma unroll
       for (int k = 0; k < PPT; ++k)
-        if (valid[k]) st_v4(static_cast<uint16_t*>(p.res_out) + row_e + pack_index(k) * 8, z[k]);
+        if (valid[k]) st_v4(static_cast<uint16_t*>(p.res_out) + row_e + gpack(k) * 8, z[k]);
     }
     const float inv = p.skip_norm ? 1.0f : rsqrtf(tot * p.inv_h + p.eps);
     uint4 y[PPT];
@@ -240,7 +309,7 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
       for (int e = 0; e < 8; ++e) yf[e] = (zf[k][e] * inv) * wv[k][e];
       y[k] = pack8<DT>(yf);
       if (p.out_f32 && valid[k]) {
-        float* o = static_cast<float*>(p.out) + row_e + pack_index(k) * 8;
+        float* o = static_cast<float*>(p.out) + row_e + gpack(k) * 8;
         st_v4(o, make_uint4(__float_as_uint(yf[0]), __float_as_uint(yf[1]), __float_as_uint(yf[2]),
                             __float_as_uint(yf[3])));
         st_v4(o + 4, make_uint4(__float_as_uint(yf[4]), __float_as_uint(yf[5]), __float_as_uint(yf[6]),
@@ -257,7 +326,7 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
     if (p.out != nullptr && !p.out_f32) {
 #pragma unroll
       for (int k = 0; k < PPT; ++k)
-        if (valid[k]) st_v4(static_cast<uint16_t*>(p.out) + row_e + pack_index(k) * 8, y[k]);
+        if (valid[k]) st_v4(static_cast<uint16_t*>(p.out) + row_e + gpack(k) * 8, y[k]);
     }
     return amax;
   };
@@ -266,7 +335,7 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
   auto quantise_row = [&](int64_t i, const float (&yq)[PPT][8], float am) {
     const int64_t row_e = out_base(i);
     const float scale = __fdiv_rn(am, 448.0f);
-    if (threadIdx.x == 0) st_f32(p.scale + row_of(i), scale);
+    if (threadIdx.x == 0 && col0 == 0) st_f32(p.scale + row_of(i), scale);  // one CTA of a cluster
     const float rcp = am == 0.0f ? 0.0f : __frcp_rn(scale);
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
@@ -277,7 +346,62 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
         for (int e = 0; e < 4; ++e)
           c[e] = e4m3x2(div_rn_by(yq[k][2 * e], scale, rcp), div_rn_by(yq[k][2 * e + 1], scale, rcp));
       }
-      st_v2(p.q + row_e + pack_index(k) * 8, make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16)));
+      st_v2(p.q + row_e + gpack(k) * 8, make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16)));
+    }
+  };
+
+  // Cluster form: combine this CTA's square-sum (and failure flag) or amax of row i with the
+  // other CTAs' (see the comment above the function); no-ops without a cluster.
+  const uint32_t me = CL ? cluster_ctarank() : 0;
+  auto cluster_sum = [&](int64_t i, float& tot, bool& failed) {
+    if constexpr (CL) {
+      const int b = (int)(i & 1);
+      if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&rx_bar[0][b], (uint32_t)(csize - 1) * 8u);
+        for (int r = 0; r < csize; ++r)
+          if (r != (int)me)
+            st_async_v2(cluster_addr(&rx_ss[b][me][0], (uint32_t)r), __float_as_uint(tot), failed ? 1u : 0u,
+                        cluster_addr(&rx_bar[0][b], (uint32_t)r));
+      }
+      const bool ok = mbar_wait_cluster_bounded(&rx_bar[0][b], (uint32_t)((i >> 1) & 1), 4 * sp.wait_cycles);
+      float t = 0.0f;
+      bool f = failed || !ok;
+      for (int r = 0; r < csize; ++r) {
+        if (r == (int)me) {
+          t += tot;
+        } else {
+          t += __uint_as_float(rx_ss[b][r][0]);
+          f = f || rx_ss[b][r][1] != 0u;
+        }
+      }
+      tot = t;
+      failed = f;
+    }
+  };
+  auto cluster_max = [&](int64_t i, float am) -> float {
+    if constexpr (CL) {
+      const int b = (int)(i & 1);
+      if (threadIdx.x == 0) {
+        mbar_arrive_expect_tx(&rx_bar[1][b], (uint32_t)(csize - 1) * 4u);
+        for (int r = 0; r < csize; ++r)
+          if (r != (int)me)
+            st_async_b32(cluster_addr(&rx_am[b][me], (uint32_t)r), __float_as_uint(am),
+                         cluster_addr(&rx_bar[1][b], (uint32_t)r));
+      }
+      const bool ok = mbar_wait_cluster_bounded(&rx_bar[1][b], (uint32_t)((i >> 1) & 1), 4 * sp.wait_cycles);
+      if (!ok && threadIdx.x == 0) atomicExch(sp.err, 1);
+      float a = 0.0f;
+      for (int r = 0; r < csize; ++r) a = fmaxf(a, r == (int)me ? am : __uint_as_float(rx_am[b][r]));
+      return a;
+    } else {
+      return am;
+    }
+  };
+  // no CTA of a cluster leaves while a store to it may still be in flight
+  auto cluster_leave = [&]() {
+    if constexpr (CL) {
+      cluster_arrive();
+      cluster_wait();
     }
   };
 
@@ -294,8 +418,10 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
       tot = block_allreduce<false>(ss, red_ss[i & 1], !ok, &failed);
     else
       failed = __syncthreads_or(!ok) != 0;
+    cluster_sum(i, tot, failed);
     if (failed) {
       fail_out(i, s, parity);
+      cluster_leave();
       return;
     }
     refill_after(i, s);
@@ -305,13 +431,13 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
         const int64_t row_e = out_base(i);
 #pragma unroll
         for (int k = 0; k < PPT; ++k) {
-          const int pk = (int)threadIdx.x + k * (int)blockDim.x;
+          const int pk = col0 + (int)threadIdx.x + k * (int)blockDim.x;
           const uint2 cw = quant_pack_per_group(zf[k], p.group_lanes, valid[k],
                                                 p.scale + row_of(i) * (int64_t)p.ngroups + pk / p.group_lanes);
           if (valid[k]) st_v2(p.q + row_e + (int64_t)pk * 8, cw);
         }
       } else {  // per token: the row's amax over the block
-        quantise_row(i, zf, block_allreduce<true>(amax, red_amax[i & 1]));
+        quantise_row(i, zf, cluster_max(i, block_allreduce<true>(amax, red_amax[i & 1])));
       }
     }
     if (++s == S) {
@@ -319,6 +445,7 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
       parity ^= 1u;
     }
   }
+  cluster_leave();
 }
 
 // The explicit minimum of one CTA per SM for 1 and 2 packs per thread lets ptxas give each
@@ -327,6 +454,14 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
 template <int DT, int N, int PPT, bool QUANT>
 __global__ void __launch_bounds__(1024 / PPT, (PPT <= 2 ? 1 : 0)) fused_staged_kernel(const FusedParams p, const StagedParams sp) {
   staged_rows<DT, N, PPT, QUANT>(p, sp, blockIdx.x, gridDim.x);
+}
+
+// Cluster form for rows longer than one CTA holds (p.csize CTAs per row, each p.chunk_packs
+// packs, PPT per thread); the grid is a whole number of clusters, each looping over rows
+// r = cluster index + i * clusters.
+template <int DT, int N, int PPT, bool QUANT>
+__global__ void __launch_bounds__(1024 / PPT, 1) fused_staged_cluster_kernel(const FusedParams p, const StagedParams sp) {
+  staged_rows<DT, N, PPT, QUANT, true>(p, sp, blockIdx.x / p.csize, gridDim.x / p.csize);
 }
 
 // ---------------------------------------------------------------------------

@@ -160,8 +160,16 @@ def options() -> List[FusedWorkload]:
                           mirror=True, group=128, seed=1241)]
 
 
+def wide_rows() -> List[FusedWorkload]:
+    """Rows longer than 8192 elements (hidden sizes of larger models), split over a cluster."""
+    return [FusedWorkload("n4_m2048_h12288_bf16_gemma_fp8", 4, 2048, 12288, gemma=True, quant=True, mirror=True,
+                          seed=1242),
+            FusedWorkload("n4_m1536_h16384_bf16_gemma_fp8", 4, 1536, 16384, gemma=True, quant=True, mirror=True,
+                          seed=1243)]
+
+
 def all_fused() -> List[FusedWorkload]:
-    return small_fused() + decode_sweep() + gemma_fp8() + large_m()
+    return small_fused() + decode_sweep() + gemma_fp8() + large_m() + wide_rows()
 
 
 def by_name(name: str):
