@@ -100,6 +100,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ar_reduce_sum.argtypes = [vp, vp, ctypes.POINTER(vp), c_int, i64, c_int, vp]
     lib.ar_fused_reduce_rmsnorm.argtypes = [vp, ctypes.POINTER(ArFusedArgs), vp]
     lib.ar_fused_reduce_rmsnorm_host.argtypes = [vp, ctypes.POINTER(ArFusedArgs), vp]
+    lib.ar_fused_reduce_rmsnorm_noalloc.argtypes = [ctypes.POINTER(ArFusedArgs), vp]
     lib.ar_status_string.argtypes = [c_int]
     lib.ar_status_string.restype = ctypes.c_char_p
     lib.ar_last_error.argtypes = [vp]
@@ -111,14 +112,18 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ar_device_status.argtypes = [vp, ctypes.POINTER(c_int)]
     lib.ar_fused_reduce_rmsnorm_batch.argtypes = [vp, ctypes.POINTER(ArFusedArgs), c_int, vp]
     for f in ("ar_init", "ar_destroy", "ar_reduce_sum", "ar_fused_reduce_rmsnorm", "ar_set_option",
-              "ar_get_info", "ar_device_status", "ar_fused_reduce_rmsnorm_batch", "ar_fused_reduce_rmsnorm_host"):
+              "ar_get_info", "ar_device_status", "ar_fused_reduce_rmsnorm_batch", "ar_fused_reduce_rmsnorm_host",
+              "ar_fused_reduce_rmsnorm_noalloc"):
         getattr(lib, f).restype = c_int
     _lib = lib
     return lib
 
 
-def status_string(status: int) -> str:
+def ar_status_string(status: int) -> str:
     return load_library().ar_status_string(int(status)).decode()
+
+
+status_string = ar_status_string
 
 
 # ---- the C ABI, one Python function per entry point -------------------------
@@ -199,6 +204,15 @@ def ar_fused_reduce_rmsnorm_host(ctx: int, args: ArFusedArgs, stream: Optional[i
     st = load_library().ar_fused_reduce_rmsnorm_host(ctx, ctypes.byref(args), stream)
     if raise_on_error:
         _check(ctx, st, "ar_fused_reduce_rmsnorm_host")
+    return st
+
+
+def ar_fused_reduce_rmsnorm_noalloc(args: ArFusedArgs, stream: Optional[int] = None,
+                                    raise_on_error: bool = True) -> int:
+    """The allocation-free form (no context; the calling thread's current device)."""
+    st = load_library().ar_fused_reduce_rmsnorm_noalloc(ctypes.byref(args), stream)
+    if raise_on_error:
+        _check(None, st, "ar_fused_reduce_rmsnorm_noalloc")
     return st
 
 

@@ -211,3 +211,9 @@ def test_host_entry_validates_like_the_device_entry(lib):
         host_st = tar.ar_fused_reduce_rmsnorm_host(None, a, None, raise_on_error=False)
         assert host_st == dev_st, (kw, host_st, dev_st)
     assert lib.ar_fused_reduce_rmsnorm_host(None, None, None) == tar.AR_ERR_INVALID_ARG
+
+
+def test_binding_has_a_function_for_every_entry_point(lib):
+    # the Python binding mirrors the C ABI name for name
+    for name in declared_functions():
+        assert hasattr(tar, name), f"no binding for {name}"
