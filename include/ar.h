@@ -65,8 +65,8 @@ typedef enum { AR_DTYPE_F32 = 0, AR_DTYPE_F16 = 1, AR_DTYPE_BF16 = 2 } ar_dtype;
  * Results; [P1] Test results runs TP2/TP4). */
 #define AR_MAX_PARTIALS 8
 
-/* FP8 epilogue modes.  PER_GROUP (SURVEY-ranked follow-up of the per-group form [P1]
- * names without a group size or scale rule): every run of group_size consecutive elements
+/* FP8 epilogue modes.  PER_GROUP (the per-group form that [P1] Changes names without a
+ * group size or scale rule, here with both fixed): every run of group_size consecutive elements
  * of a row gets its own scale amax_group / 448 and codes by the per-token rules; scales
  * are [m, h / group_size] fp32 row-major. */
 enum { AR_QUANT_NONE = 0, AR_QUANT_FP8_E4M3_PER_TOKEN = 1, AR_QUANT_FP8_E4M3_PER_GROUP = 2 };
@@ -175,8 +175,8 @@ ar_status ar_device_status(ar_ctx* ctx, int* code);
 
 /*
  * Several independent fused calls in one launch, so a batch of decode-sized calls pays
- * one launch instead of `count` (SURVEY-ranked follow-up of the interleaved small and
- * large fused calls on [P1] Changes).
+ * one launch instead of `count` (for the interleaved small and large fused calls that
+ * [P1] Changes describes).
  *
  * calls: host array of `count` (1..AR_MAX_BATCH) argument blocks, each valid for
  * ar_fused_reduce_rmsnorm on its own and all with the same n, dtype, quant, skip_norm and
