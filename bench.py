@@ -389,6 +389,23 @@ def oracle_sample_us(wl, rows: int):
     return dt * 1e6 * (wl.m / rows), rows
 
 
+def cpu_model() -> str:
+    """The host CPU as /proc/cpuinfo names it (model name, else implementer and part)."""
+    info = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                k, _, v = line.partition(":")
+                info.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if info.get("model name"):
+        return info["model name"]
+    if info.get("CPU part"):
+        return f"{os.uname().machine} (implementer {info.get('CPU implementer', '?')}, part {info['CPU part']})"
+    return os.uname().machine
+
+
 def host_cores() -> int:
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
@@ -442,10 +459,14 @@ def cpu_baseline(wl, seconds: float = 12.0, runs: int = 5):
         if pinned:
             os.sched_setaffinity(0, cpus)
     mt_us, cores, mt_rows = oracle_all_cores_us(wl)
-    return {"value": statistics.median(samples), "unit": UNIT, "cores": 1, "kind": "oracle",
+    value = statistics.median(samples)
+    fp = wl.algorithmic_bytes()
+    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "cpu": cpu_model(),
+            "gbs": round(fp / (value * 1e-6) / 1e9, 4),
             "sample": f"serial C oracle on {rows} of {wl.m} rows, one thread pinned to one core, median of "
                       f"{runs} runs, scaled to a full call",
             "all_cores": {"value": round(mt_us, 3), "unit": UNIT, "cores": cores,
+                          "gbs": round(fp / (mt_us * 1e-6) / 1e9, 4),
                           "sample": f"the same oracle, {mt_rows} of {wl.m} rows split in {cores} row blocks "
                                     f"over {cores} threads, median of 3 runs, scaled to a full call"}}
 
@@ -468,7 +489,8 @@ def run_reference(args, world, rank):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sum(times) / len(times) / 1000, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
             "data": "synthetic", "config": {"workload": wl.name, "n_partials": wl.n, "m": wl.m, "h": wl.h},
-            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "cpu": cpu_model(),
+                             "sample": sample},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
