@@ -50,10 +50,16 @@ def dist_env():
     return world, rank, local
 
 
-def init_dist(world: int, backend: str):
+def init_dist(world: int, backend: str, timeout_s: float | None = None):
+    """Join the replicas' process group.  A bounded timeout (default 600 s, or
+    AR_BENCH_PG_TIMEOUT seconds) turns a rank that died or never arrives into an error at the
+    next barrier or reduction on the others, instead of a wait of torch's default length."""
+    import datetime
     import torch.distributed as dist
     if world > 1 and not dist.is_initialized():
-        dist.init_process_group(backend)
+        if timeout_s is None:
+            timeout_s = float(os.environ.get("AR_BENCH_PG_TIMEOUT", "600"))
+        dist.init_process_group(backend, timeout=datetime.timedelta(seconds=timeout_s))
     return dist
 
 

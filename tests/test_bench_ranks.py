@@ -86,3 +86,35 @@ def test_cpu_baseline_reports_serial_and_all_cores():
     cpu = bench.cpu_baseline(wl, seconds=0.3)
     assert cpu["kind"] == "oracle" and cpu["cores"] == 1 and cpu["value"] > 0
     assert cpu["all_cores"]["cores"] == cores and cpu["all_cores"]["unit"] == cpu["unit"]
+
+
+def _leaving_worker(rank, world, port, q):
+    import time
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    dist = bench.init_dist(world, "gloo", timeout_s=20)
+    if rank == 1:
+        os._exit(0)                      # leaves between steps, without joining the barrier
+    t0 = time.time()
+    try:
+        bench.barrier(world)
+        q.put(("no error", time.time() - t0))
+    except Exception as e:               # the survivor learns of it as an error, not a hang
+        q.put((type(e).__name__, time.time() - t0))
+    os._exit(0)
+
+
+def test_a_rank_that_leaves_is_an_error_on_the_other():
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    ps = [ctx.Process(target=_leaving_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    kind, waited = q.get(timeout=120)
+    for p in ps:
+        p.join(timeout=60)
+    assert kind != "no error"
+    assert waited < 60
