@@ -100,7 +100,10 @@ ar_status ar_destroy(ar_ctx* ctx);
  * dtype:    AR_DTYPE_F32, AR_DTYPE_F16 or AR_DTYPE_BF16 (fp32: the fp32 sum is stored).
  * stream:   cudaStream_t (NULL = legacy default stream).
  * Pointers must be aligned to the element size; 16-byte-aligned pointers take the vector
- * path, others a scalar path with the same results.
+ * path, others a scalar path with the same results.  Large 16-bit arrays of 4 to 6
+ * partials (at least 131072 elements per SM, a multiple of a row length of 2048..8192)
+ * are summed by the staged fused kernel on the array viewed as rows, without residual or
+ * norm: the same bits.
  */
 ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int n, int64_t numel,
                         ar_dtype dtype, void* stream);
@@ -165,9 +168,10 @@ typedef struct {
 ar_status ar_fused_reduce_rmsnorm(ar_ctx* ctx, const ar_fused_args* args, void* stream);
 
 /*
- * Read and clear the context's device status word.  The staged variant waits on its
- * shared-memory copies with a bound (about a second); if a wait ever runs out, the kernel
- * stops early, its outputs are incomplete, and it records code 1 here.  0 means no wait
+ * Read and clear the context's device status word.  The staged variants wait on their
+ * shared-memory copies (and, in the cluster form, on the peer CTAs' totals) with a bound
+ * (about a second); if a wait ever runs out, the kernel stops early, its outputs are
+ * incomplete, and it records code 1 here.  0 means no wait
  * has run out since the last read.  Synchronises the device (a blocking copy): call it
  * outside graph capture, e.g. after a batch of calls.  No counterpart on the pages.
  */
