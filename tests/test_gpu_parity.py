@@ -5,8 +5,9 @@ benchmark uses), the shape list of the fused-kernel test on page "[HIP] fix(cust
 gfx1250 fused all-reduce + RMSNorm" (Changes / test command), the tail cases of page "[HIP]
 [Perf] Specialize partial tiles in two-stage custom all-reduce" (1023/1024/1025 x 512,
 tails of 1/63/64/65/127 packs, byte sizes around 1 MiB), every kernel variant, N = 1..8,
-both element types, aliases, misaligned pointers and empty inputs.  Outputs sit between
-sentinel guard regions and are poisoned before each call.
+both element types, aliases, misaligned pointers, empty inputs and the maximum sizes (the
+longest rows accepted and the first refused; 2^20 rows in one call, checked on sampled rows).
+Outputs sit between sentinel guard regions and are poisoned before each call.
 """
 import numpy as np
 import pytest
@@ -407,3 +408,44 @@ def test_reduce_empty(ctx, dev):
     parts = [torch.empty(0, dtype=torch.bfloat16, device=dev) for _ in range(3)]
     ctx.reduce_sum(parts)
     assert ctx.last_variant == "none"
+
+
+# ---------------------------------------------------------------------------
+# maximum sizes
+# ---------------------------------------------------------------------------
+
+def test_longest_rows(ctx, dev, orc):
+    """The longest rows a call accepts: 1024 packs per CTA times the largest cluster (16 CTAs
+    where the device allows non-portable clusters, else 8); one pack more is refused."""
+    longest = None
+    for h in (131072, 65536):
+        inp = synth.fused_inputs(2, 3, h, "bf16", seed=h % 997, gemma=True)
+        try:
+            got = run_fused(ctx, dev, inp, "bf16", gemma=True, quant=True)
+        except tar.ArError as e:
+            assert e.status == tar.AR_ERR_UNSUPPORTED and h == 131072
+            continue
+        check_fused(orc, got, oracle_fused(orc, inp, "bf16", gemma=True, quant=True), "bf16", True)
+        longest = h
+        break
+    assert longest is not None
+    inp = synth.fused_inputs(2, 2, longest + 8, "bf16", seed=5)
+    with pytest.raises(tar.ArError) as e:
+        run_fused(ctx, dev, inp, "bf16")
+    assert e.value.status == tar.AR_ERR_UNSUPPORTED
+
+
+def test_tall_call_sampled_rows(ctx, dev, orc):
+    """2^20 rows of 64 elements in one call (the persistent staged kernel runs hundreds of rows
+    per CTA): rows are independent, so sampled rows are checked against the oracle run on
+    those rows alone, FP8 included."""
+    m, h, n = 1 << 20, 64, 2
+    inp = synth.fused_inputs(n, m, h, "bf16", seed=17, gemma=True)
+    got = run_fused(ctx, dev, inp, "bf16", gemma=True, quant=True)
+    assert got["variant"] == "fused_staged"
+    rows = np.unique(np.concatenate([np.arange(0, m, 4099), np.arange(m - 300, m)]))
+    sub = {"partials": [p[rows] for p in inp["partials"]], "residual": inp["residual"][rows],
+           "weight": inp["weight"]}
+    ref = oracle_fused(orc, sub, "bf16", gemma=True, quant=True)
+    pick = {k: (v[rows] if v is not None and k != "variant" else v) for k, v in got.items()}
+    check_fused(orc, pick, ref, "bf16", True)
