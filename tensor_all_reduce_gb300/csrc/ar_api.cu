@@ -478,7 +478,6 @@ static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, b
 
   const int es = elem_size(a->dtype);
   const int oes = a->out_fp32 ? 4 : es;  // element size of `out`
-  const int64_t mh = a->m * a->h;
   const int64_t ext_in = (a->m - 1) * li + a->h;   // elements an input spans (padding included)
   const int64_t ext_out = (a->m - 1) * lo + a->h;  // elements an output spans
   const int64_t tb = ext_in * es;                  // bytes of one input [m, h] tensor
@@ -518,7 +517,6 @@ static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, b
   // ---- variant selection ----
   // the vector kernels need 16-byte-aligned rows: h, and both row strides, multiples of 8
   bool vec = (a->h % 8) == 0 && (li % 8) == 0 && (lo % 8) == 0;
-  (void)mh;
   for (int r = 0; r < a->n; ++r) vec = vec && aligned(a->partials[r], 16);
   vec = vec && (!a->residual_in || aligned(a->residual_in, 16)) && (!a->residual_out || aligned(a->residual_out, 16)) &&
         aligned(a->weight, 16) && (!a->out || aligned(a->out, 16)) && (!quant || aligned(a->q_out, 8));
