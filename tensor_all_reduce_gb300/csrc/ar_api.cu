@@ -664,11 +664,10 @@ static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, b
   if (!host && (ctx->force_variant == 3 || (staged_auto && staged_ok))) {
     if (!staged_ok) return AR_ERR_UNSUPPORTED;
     // packs per thread: 1 (768 threads for h = 6144) when each CTA runs through many rows
-    // with the norm and at most 4 partials, else 2 (same A/B runs: 1 pack was 0.4-1 % faster
-    // on N = 4, 2800 x 6144 with per-token FP8, without FP8 and with fp32 output; 2 packs on
-    // 1024 rows, on N = 8, without the norm and with per-group FP8)
-    const bool one_pack =
-        a->n <= 4 && !a->skip_norm && !per_group && a->m >= 8LL * ctx->sm_count && row_packs <= 1024;
+    // with the norm and at most 4 partials, else 2 (same A/B runs: 1 pack was 0.5-1 % faster
+    // on N = 4, 2800 x 6144 with per-token and per-group FP8, without FP8 and with fp32
+    // output; 2 packs on 1024 rows, on N = 8 and without the norm)
+    const bool one_pack = a->n <= 4 && !a->skip_norm && a->m >= 8LL * ctx->sm_count && row_packs <= 1024;
     const int sppt = ctx->ppt ? ctx->ppt : (one_pack ? 1 : 2);
     int sblock = ((row_packs + sppt - 1) / sppt + 31) / 32 * 32;
     if (sblock < 32) sblock = 32;

@@ -177,6 +177,27 @@ __device__ __forceinline__ void unpack8(const uint4& v, float (&f)[8]) {
   }
 }
 
+// acc[e] = acc[e] + (float)x_e for the 8 16-bit values x of a pack, with mixed-precision
+// adds (a 16-bit operand, an fp32 operand and result): the conversion to fp32 is exact, so
+// each sum is the same single fp32 rounding as converting first and adding.
+template <int DT>
+__device__ __forceinline__ void add8(float (&acc)[8], const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if constexpr (DT == kBF16)
+      asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+          "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+          : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1])
+          : "r"(w[i]));
+    else
+      asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+          "add.rn.f32.f16 %0, lo, %0;\n\tadd.rn.f32.f16 %1, hi, %1;\n\t}"
+          : "+f"(acc[2 * i]), "+f"(acc[2 * i + 1])
+          : "r"(w[i]));
+  }
+}
+
 template <int DT>
 __device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
   uint4 v;

@@ -241,23 +241,17 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
       const int pkc = valid[k] ? (int)pack_index(k) : 0;
+      // rank order: acc = x_0, then acc + x_1, ..., each an fp32 sum of an exact conversion
       float acc[8];
       unpack8<DT>(lds_v4(st + (size_t)pkc * 16), acc);
 #pragma unroll
-      for (int r = 1; r < N; ++r) {
-        float t[8];
-        unpack8<DT>(lds_v4(st + (size_t)r * row_bytes + (size_t)pkc * 16), t);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[e] = acc[e] + t[e];
-      }
+      for (int r = 1; r < N; ++r) add8<DT>(acc, lds_v4(st + (size_t)r * row_bytes + (size_t)pkc * 16));
       uint4 sv = pack8<DT>(acc);
-      if (has_res) {
-        float sf[8], rf[8];
-        unpack8<DT>(sv, sf);
+      if (has_res) {  // z = round(res + s): the residual converted, the rounded sum added to it
+        float rf[8];
         unpack8<DT>(lds_v4(st + (size_t)N * row_bytes + (size_t)pkc * 16), rf);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) sf[e] = sf[e] + rf[e];
-        sv = pack8<DT>(sf);
+        add8<DT>(rf, sv);
+        sv = pack8<DT>(rf);
       }
       z[k] = sv;
       unpack8<DT>(sv, zf[k]);
