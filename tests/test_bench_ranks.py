@@ -94,9 +94,14 @@ def _leaving_worker(rank, world, port, q):
                       LOCAL_RANK=str(rank))
     sys.path.insert(0, ROOT)
     import bench
-    dist = bench.init_dist(world, "gloo", timeout_s=20)
+    try:
+        bench.init_dist(world, "gloo", timeout_s=20)
+        bench.barrier(world)             # one step done together
+    except Exception as e:
+        q.put(("setup failed: " + type(e).__name__, -1.0))
+        os._exit(0)
     if rank == 1:
-        os._exit(0)                      # leaves between steps, without joining the barrier
+        os._exit(0)                      # leaves between steps, without joining the next barrier
     t0 = time.time()
     try:
         bench.barrier(world)
@@ -109,12 +114,14 @@ def _leaving_worker(rank, world, port, q):
 def test_a_rank_that_leaves_is_an_error_on_the_other():
     port = _free_port()
     ctx = mp.get_context("spawn")
-    q = ctx.Queue()
+    q = ctx.SimpleQueue()                # put() writes synchronously: safe before os._exit
     ps = [ctx.Process(target=_leaving_worker, args=(r, 2, port, q)) for r in range(2)]
     for p in ps:
         p.start()
-    kind, waited = q.get(timeout=120)
     for p in ps:
-        p.join(timeout=60)
+        p.join(timeout=120)
+    assert not q.empty(), "the surviving rank reported nothing"
+    kind, waited = q.get()
+    assert not kind.startswith("setup failed"), kind
     assert kind != "no error"
-    assert waited < 60
+    assert 0 <= waited < 60
