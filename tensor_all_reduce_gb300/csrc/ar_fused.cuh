@@ -43,6 +43,20 @@ __device__ __forceinline__ void load_pack(const void* base, int64_t e0, int64_t 
   }
 }
 
+// acc[i] = acc[i] + x_i for the pack at base[e0 .. e0 + 8) (in the element-wise form,
+// elements at or beyond `limit` count as 0): each sum is one fp32 rounding of an exact
+// conversion, as mixed-precision adds in the vector form.
+template <int DT, bool VEC, bool STREAM>
+__device__ __forceinline__ void load_add_pack(const void* base, int64_t e0, int64_t limit, float (&acc)[8]) {
+  const uint16_t* b = static_cast<const uint16_t*>(base);
+  if constexpr (VEC) {
+    add8<DT>(acc, STREAM ? ld_stream(b + e0) : ld_keep(b + e0));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = acc[i] + ((e0 + i < limit) ? to_f32<DT>(ld_u16(b + e0 + i)) : 0.0f);
+  }
+}
+
 // Store one pack of 16-bit values (already rounded, packed in a uint4).
 template <bool VEC>
 __device__ __forceinline__ void store_pack(void* base, int64_t e0, int64_t limit, const uint4& v) {
@@ -108,20 +122,13 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
     float acc[8];
     load_pack<DT, VEC, true>(p.x[0], e0, lim, acc);
 #pragma unroll
-    for (int r = 1; r < N; ++r) {
-      float t[8];
-      load_pack<DT, VEC, true>(p.x[r], e0, lim, t);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = acc[i] + t[i];  // fp32, rank order 0..N-1
-    }
+    for (int r = 1; r < N; ++r) load_add_pack<DT, VEC, true>(p.x[r], e0, lim, acc);  // fp32, rank order
     uint4 s = pack8<DT>(acc);                              // one rounding to T
-    if (p.res_in != nullptr) {
-      float sf[8], rf[8];
-      unpack8<DT>(s, sf);
+    if (p.res_in != nullptr) {                             // z = round(res + s)
+      float rf[8];
       load_pack<DT, VEC, true>(p.res_in, e0, lim, rf);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) sf[i] = sf[i] + rf[i];
-      s = pack8<DT>(sf);                                   // second rounding to T
+      add8<DT>(rf, s);
+      s = pack8<DT>(rf);                                   // second rounding to T
     }
     z[k] = s;
     // weight row: 8 consecutive entries starting at column pkc * 8 (none without the norm)
