@@ -151,13 +151,23 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source with comments removed and whitespace collapsed (what the compiler sees)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the library's sources, comments and layout left out, so that a recorded DRAM
+    traffic figure stays attached to the code it was measured on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "tensor_all_reduce_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
         if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+            with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+                h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,17 +1,17 @@
-// Staged large-M variant of the fused kernel: persistent CTAs, bulk asynchronous copies of
-// whole rows into shared memory, S-deep pipeline.
+// Staged variant of the fused kernel: persistent CTAs, bulk asynchronous copies of whole
+// rows (or, in the cluster form, of each CTA's slice of every row) into shared memory,
+// S-deep pipeline.
 //
 // Same arithmetic as fused_kernel (ar_fused.cuh); only the data movement differs.  The
 // grid holds as many CTAs as fit on the SMs at once (their shared-memory rings set the
 // count); each loops over rows r = blockIdx.x + i * gridDim.x.  For each row one thread
-// issues a bulk global->shared copy (cp.async.bulk, the non-tensor form of TMA) of the
-// N partial rows and the residual row into stage i % S and arms the stage's mbarrier with
+// issues bulk global->shared copies (cp.async.bulk, the non-tensor form of TMA) of the N
+// partial rows and the residual row into stage i % S and arms the stage's mbarrier with
 // the byte count; while the CTA works on row i, rows i+1 .. i+S-1 are in flight (with
-// S = 1 the next row's copy is issued as soon as the current row's square-sum is known and
-// overlaps the rest of its work, and other CTAs on the SM fill the gaps).  A stage
-// is refilled as soon as the row's square-sum has been reduced (by then every thread has
-// read its packs), so loads for later rows overlap the normalisation and the stores.
-// The weight packs a thread needs never change across rows and live in registers.
+// S = 1, used when every row has its own CTA, the copy is the row's only one).  A stage is
+// refilled as soon as the row's square-sum has been reduced (by then every thread has read
+// its packs), so loads for later rows overlap the normalisation and the stores.  The
+// weight packs a thread needs never change across rows and live in registers.
 //
 // Full tiles only (page "[HIP] [Perf] Specialize partial tiles in two-stage custom
 // all-reduce", Proposed modifications: every thread executes the same number of
@@ -20,8 +20,8 @@
 //
 // Waits are bounded: a wait on a stage's mbarrier gives up after `wait_cycles` SM clock
 // cycles, the CTA agrees on the failure in the row's square-sum barrier (an OR-reduction
-// in the same barrier), records code 1 in `err`,
-// waits (bounded again) for its own copies still in flight, and returns.
+// in the same barrier), records code 1 in `err`, waits (bounded again) for its own copies
+// still in flight, and returns.
 #pragma once
 
 #include "ar_common.cuh"
