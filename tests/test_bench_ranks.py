@@ -125,3 +125,31 @@ def test_a_rank_that_leaves_is_an_error_on_the_other():
     assert not kind.startswith("setup failed"), kind
     assert kind != "no error"
     assert 0 <= waited < 60
+
+
+def test_reference_arm_line_single_process():
+    env = dict(os.environ, PYTHONPATH=ROOT)
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        env.pop(k, None)
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "3", "--warmup", "3",
+           "--workload", "n4_m16_h6144_bf16_plain"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads([x for x in r.stdout.splitlines() if x.startswith("{")][-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["steps"] == 3 and line["n_gpus"] == 1
+    assert line["cpu_baseline"]["cores"] == 1 and line["cpu_baseline"]["cpu"]
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    sys.path.insert(0, ROOT)
+    import bench
+    a = "int f(int x) { // add one\n  return x + 1; /* done */ }\n"
+    b = "int f(int x) {\n    return x + 1;\n}\n"
+    c = "int f(int x) { return x + 2; }"
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only(a) != bench._code_only(c)
+    assert len(bench.kernel_source_hash()) == 16
