@@ -217,3 +217,38 @@ def test_binding_has_a_function_for_every_entry_point(lib):
     # the Python binding mirrors the C ABI name for name
     for name in declared_functions():
         assert hasattr(tar, name), f"no binding for {name}"
+
+
+def test_header_compiles_and_links_as_plain_c(lib, tmp_path):
+    """include/ar.h is a C header: a C11 program compiles against it (warnings as errors) and
+    links to libar.so; it runs only the calls that need no GPU."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "abi.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "ar.h"
+int main(void) {
+  ar_fused_args a;
+  memset(&a, 0, sizeof a);
+  a.n = 1; a.h = 0; a.dtype = AR_DTYPE_BF16;            /* h = 0: refused before anything else */
+  if (ar_fused_reduce_rmsnorm(NULL, &a, NULL) != AR_ERR_INVALID_ARG) return 1;
+  if (ar_fused_reduce_rmsnorm_host(NULL, &a, NULL) != AR_ERR_INVALID_ARG) return 2;
+  if (ar_destroy(NULL) != AR_OK) return 3;
+  if (strcmp(ar_status_string(AR_OK), "success") != 0) return 4;
+  if (ar_reduce_sum(NULL, NULL, NULL, 0, 0, AR_DTYPE_F32, NULL) != AR_ERR_INVALID_ARG) return 5;
+  printf("ok %d\n", AR_MAX_PARTIALS);
+  return 0;
+}
+''')
+    libdir = os.path.dirname(tar.LIB_PATH)
+    exe = tmp_path / "abi"
+    r = subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I", os.path.join(ROOT, "include"),
+                        str(src), "-L", libdir, "-lar", f"-Wl,-rpath,{libdir}", "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == f"ok {tar.AR_MAX_PARTIALS}", (r.returncode, r.stdout, r.stderr)
