@@ -400,3 +400,15 @@ def test_fused_with_per_group_quant(orc, dtype):
     ref = orc.fused(ps, res, w, 1e-6, True, True, dtype)
     assert np.array_equal(out["y"], ref["y"]) and np.array_equal(out["res_out"], ref["res_out"])
 
+
+
+def test_per_group_hand_worked_row(orc):
+    """Per-group FP8 of a hand-worked 1 x 16 bf16 row in two groups of 8
+    (tests/golden/worked_group8_1x16.json, derived from the format definitions)."""
+    import json
+    import os
+    fx = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_group8_1x16.json")))
+    y = np.array([int(b, 16) for b in fx["inputs"]["y_bf16_bits"]], dtype=np.uint16).reshape(1, 16)
+    q, sc = orc.per_group_quant(y, fx["inputs"]["group"], "bf16")
+    assert [f"0x{v:08x}" for v in sc.view(np.uint32).ravel()] == fx["expected"]["scale_f32_bits"]
+    assert [f"0x{v:02x}" for v in q.ravel()] == fx["expected"]["q_e4m3"]
