@@ -94,21 +94,28 @@ class ReduceCall:
 
 def test_graph_interleaved_calls(dev, orc):
     calls = [
-        FusedCall(dev, 4, 16, 6144, "bf16", False, False),     # decode-sized: cluster split
+        FusedCall(dev, 4, 16, 6144, "bf16", False, False),     # decode-sized: one staged CTA per row
         ReduceCall(dev, 4, 1025 * 512, "fp16"),                 # tail path
-        FusedCall(dev, 4, 384, 6144, "bf16", True, True),       # FP8 epilogue
+        FusedCall(dev, 4, 384, 6144, "bf16", True, True),       # FP8 epilogue, persistent staged
         FusedCall(dev, 4, 1, 6144, "bf16", False, False),      # one token
         ReduceCall(dev, 4, 1024 * 512, "fp32"),
-        FusedCall(dev, 8, 1024, 6144, "bf16", False, False),    # large M: row per CTA
-        FusedCall(dev, 4, 7, 6145, "fp16", True, True),         # tail hidden size
+        FusedCall(dev, 8, 1024, 6144, "bf16", False, False),    # large M
+        FusedCall(dev, 4, 7, 6145, "fp16", True, True),         # tail hidden size: element-wise form
+        FusedCall(dev, 4, 64, 12288, "bf16", True, True),       # long rows: staged cluster form
+        ReduceCall(dev, 5, 8192 * 16 * 152, "bf16"),            # large 16-bit sum: staged rows
     ]
     with tar.Context(0) as ctx:
         for i, c in enumerate(calls):
             c.load(seed=i)
         # eager warm-up, then capture on a side stream
+        ran = []
         for c in calls:
             c.call(ctx)
+            ran.append(ctx.last_variant)
         torch.cuda.synchronize()
+        assert ran[0] == "fused_staged" and "scalar" in ran[6] and ran[7] == "fused_staged_cluster", ran
+        if ctx.info(tar.AR_INFO_SM_COUNT) <= 152:
+            assert ran[8] == "reduce_staged", ran
         g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
         s.wait_stream(torch.cuda.current_stream())
