@@ -1,11 +1,13 @@
 """Fused N-way partial reduce + residual add + RMSNorm (+ per-token FP8 E4M3) on GB300.
 
 A thin ctypes binding over ``libar.so`` (see ``include/ar.h``).  The functions named like
-the C ABI (``ar_init``, ``ar_reduce_sum``, ``ar_fused_reduce_rmsnorm``, ``ar_destroy`` ...)
-take raw device pointers and sizes exactly as the C functions do; ``reduce_sum`` and
-``fused_reduce_rmsnorm`` marshal torch tensors into those calls.  Every step of the
-computation runs in the library's CUDA kernels: there is no Python or PyTorch compute
-path, and using the package without a built ``libar.so`` raises.
+the C ABI (``ar_init``, ``ar_reduce_sum``, ``ar_fused_reduce_rmsnorm``,
+``ar_fused_reduce_rmsnorm_batch``, ``ar_fused_reduce_rmsnorm_host``,
+``ar_fused_reduce_rmsnorm_noalloc``, ``ar_destroy`` ...) take raw pointers and sizes exactly
+as the C functions do; the ``Context`` methods (``reduce_sum``, ``fused_reduce_rmsnorm``,
+``fused_reduce_rmsnorm_batch``, ``fused_reduce_rmsnorm_host``) marshal torch tensors into
+those calls.  Every step of the computation runs in the library's CUDA kernels: there is no
+Python or PyTorch compute path, and using the package without a built ``libar.so`` raises.
 """
 from __future__ import annotations
 
