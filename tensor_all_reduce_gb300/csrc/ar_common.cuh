@@ -220,16 +220,53 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
 // "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
 // Dev. 34(1), 1990): q0 = RN(y r) is within an ulp of y / d, the remainder y - q0 d is
 // exact through the fused multiply-add, and RN(q0 + rem r) is RN(y / d) when r is the
-// correctly rounded reciprocal and the quotient is in the normal range.  A binary quotient
-// is never exactly half-way between two floats, so there are no ties to break.  Used for
-// the per-element FP8 quotient, where it replaces an IEEE division per element by three
-// multiply-adds; quotients below the normal range round to FP8 zero either way.  The
-// correction of a zero quotient would return +0 for y = -0 ((+0) + (-0) = +0), so the
-// sign is taken from y, as IEEE division keeps it.
+// correctly rounded reciprocal of a normal d and neither the remainder nor the quotient
+// leaves the normal range.  A binary quotient is never exactly half-way between two floats,
+// so there are no ties to break.  The correction of a zero quotient would return +0 for
+// y = -0 ((+0) + (-0) = +0), so the sign is taken from y, as IEEE division keeps it.
 __device__ __forceinline__ float div_rn_by(float y, float d, float r) {
   const float q0 = y * r;
   const float rem = fmaf(-q0, d, y);
   return copysignf(fmaf(rem, r, q0), y);
+}
+
+// Smallest row (or group) maximum for which the FP8 quotients take div_rn_by.  With
+// amax >= 2^-80: scale = RN(amax / 448) >= 2^-89 is normal and 1 / scale <= 2^89 finite;
+// a quotient that can reach a nonzero E4M3 code (|y / scale| >= 2^-10, half the smallest
+// subnormal code) has |y| >= 2^-99, so the remainder is a multiple of at least 2^-146 and
+// exact; smaller quotients round to code 0 both ways (q0 <= 2^-10 and the correction of a
+// quotient below 2^-10 is not positive).  Below this bound (bf16 rows or groups of tiny
+// values; an fp16 maximum is at least 2^-24) scale can be subnormal and its reciprocal
+// infinite, so each quotient is an IEEE binary32 division instead.
+constexpr float kFp8ReciprocalMinAmax = 0x1p-80f;
+
+// How the FP8 codes of one row or group with maximum magnitude `am` are formed.
+struct Fp8Scale {
+  float scale;  // RN(am / 448), the stored scale
+  float rcp;    // RN(1 / scale) when mode == 1
+  int mode;     // 0: am == 0, every code 0 (no division); 1: div_rn_by; 2: IEEE division
+};
+
+__device__ __forceinline__ Fp8Scale fp8_scale(float am) {
+  Fp8Scale s;
+  s.scale = __fdiv_rn(am, 448.0f);
+  s.mode = am == 0.0f ? 0 : (am >= kFp8ReciprocalMinAmax ? 1 : 2);
+  s.rcp = s.mode == 1 ? __frcp_rn(s.scale) : 0.0f;
+  return s;
+}
+
+// E4M3 codes (saturating, round-to-nearest-even) of y / scale for 8 rounded values y, in
+// address order (element 0 in the lowest byte).
+__device__ __forceinline__ uint2 fp8_codes8(const float (&y)[8], const Fp8Scale& s) {
+  uint32_t c[4] = {0u, 0u, 0u, 0u};
+  if (s.mode == 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = e4m3x2(div_rn_by(y[2 * i], s.scale, s.rcp), div_rn_by(y[2 * i + 1], s.scale, s.rcp));
+  } else if (s.mode == 2) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) c[i] = e4m3x2(__fdiv_rn(y[2 * i], s.scale), __fdiv_rn(y[2 * i + 1], s.scale));
+  }
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
 // Per-group FP8 of one pack of 8 rounded values y, in groups of `lanes` consecutive packs
@@ -241,17 +278,9 @@ __device__ __forceinline__ uint2 quant_pack_per_group(const float (&y)[8], int l
 #pragma unroll
   for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(y[i]));
   for (int o = 1; o < lanes; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  const float scale = __fdiv_rn(a, 448.0f);
-  if (store && (threadIdx.x & (unsigned)(lanes - 1)) == 0) st_f32(scale_slot, scale);
-  const float rcp = a == 0.0f ? 0.0f : __frcp_rn(scale);
-  uint32_t c[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float q0 = a == 0.0f ? 0.0f : div_rn_by(y[2 * i], scale, rcp);
-    const float q1 = a == 0.0f ? 0.0f : div_rn_by(y[2 * i + 1], scale, rcp);
-    c[i] = e4m3x2(q0, q1);
-  }
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+  const Fp8Scale s = fp8_scale(a);
+  if (store && (threadIdx.x & (unsigned)(lanes - 1)) == 0) st_f32(scale_slot, s.scale);
+  return fp8_codes8(y, s);
 }
 
 // ---------------------------------------------------------------------------

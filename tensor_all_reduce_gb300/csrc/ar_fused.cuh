@@ -229,30 +229,23 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
       if (threadIdx.x == 0) slot_amax = am;
       am = cluster_gather<true>(&slot_amax, &bcast, csize);
     }
-    const float scale = __fdiv_rn(am, 448.0f);
-    if (crank == 0 && threadIdx.x == 0) st_f32(p.scale + row, scale);
-    // an all-zero row has scale 0 and all codes 0 (no division)
-    const float rcp = am == 0.0f ? 0.0f : __frcp_rn(scale);
+    const Fp8Scale fs = fp8_scale(am);  // an all-zero row has scale 0 and all codes 0
+    if (crank == 0 && threadIdx.x == 0) st_f32(p.scale + row, fs.scale);
 #pragma unroll
     for (int k = 0; k < PPT; ++k) {
       if (!valid[k]) continue;
       const int pk = pk_begin + (int)threadIdx.x + k * (int)blockDim.x;
       float yr[8];
       unpack8<DT>(y[k], yr);
-      uint32_t c[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float a = am == 0.0f ? 0.0f : div_rn_by(yr[2 * i], scale, rcp);
-        const float b = am == 0.0f ? 0.0f : div_rn_by(yr[2 * i + 1], scale, rcp);
-        c[i] = e4m3x2(a, b);
-      }
+      const uint2 cw = fp8_codes8(yr, fs);
       const int64_t e0 = row_e + (int64_t)pk * 8;
       if constexpr (VEC) {
-        st_v2(p.q + e0, make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16)));
+        st_v2(p.q + e0, cw);
       } else {
+        const uint32_t c2[2] = {cw.x, cw.y};
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-          if (e0 + i < row_end) st_u8(p.q + e0 + i, (uint8_t)((c[i >> 1] >> (8 * (i & 1))) & 0xFFu));
+          if (e0 + i < row_end) st_u8(p.q + e0 + i, (uint8_t)((c2[i >> 2] >> (8 * (i & 3))) & 0xFFu));
       }
     }
   }

@@ -328,20 +328,11 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
   // Per-token FP8 codes of row i from its rounded y and the row's amax.
   auto quantise_row = [&](int64_t i, const float (&yq)[PPT][8], float am) {
     const int64_t row_e = out_base(i);
-    const float scale = __fdiv_rn(am, 448.0f);
-    if (threadIdx.x == 0 && col0 == 0) st_f32(p.scale + row_of(i), scale);  // one CTA of a cluster
-    const float rcp = am == 0.0f ? 0.0f : __frcp_rn(scale);
+    const Fp8Scale fs = fp8_scale(am);  // an all-zero row keeps codes 0 (no division)
+    if (threadIdx.x == 0 && col0 == 0) st_f32(p.scale + row_of(i), fs.scale);  // one CTA of a cluster
 #pragma unroll
-    for (int k = 0; k < PPT; ++k) {
-      if (!valid[k]) continue;
-      uint32_t c[4] = {0u, 0u, 0u, 0u};  // an all-zero row keeps codes 0 (no division)
-      if (am != 0.0f) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          c[e] = e4m3x2(div_rn_by(yq[k][2 * e], scale, rcp), div_rn_by(yq[k][2 * e + 1], scale, rcp));
-      }
-      st_v2(p.q + row_e + gpack(k) * 8, make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16)));
-    }
+    for (int k = 0; k < PPT; ++k)
+      if (valid[k]) st_v2(p.q + row_e + gpack(k) * 8, fp8_codes8(yq[k], fs));
   };
 
   // Cluster form: combine this CTA's square-sum (and failure flag) or amax of row i with the

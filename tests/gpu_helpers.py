@@ -70,8 +70,10 @@ def assert_fp8(orc, q: np.ndarray, scale: np.ndarray, y_gpu_bits: np.ndarray, dt
         tol = 2.0 ** -7 if dtype == "bf16" else 2.0 ** -10
         r2 = np.abs(scale.astype(np.float64) - ref["scale"]) / np.maximum(ref["scale"].astype(np.float64), 1e-300)
         assert np.all(same | (r2 <= tol * 1.0001)), f"{what}: scale differs from the oracle beyond 1 ulp of amax"
-        d2 = np.abs(code_ordinal(q[same]) - code_ordinal(ref["q"][same]))
-        assert d2.max(initial=0) <= 1, f"{what}: codes differ from the oracle by {d2.max()} on equal-scale rows"
+        # every code within one code of the oracle's own (a scale off by one ulp of amax and a
+        # y off by one ulp move a quotient by less than half an E4M3 step)
+        d2 = np.abs(code_ordinal(q) - code_ordinal(ref["q"]))
+        assert d2.max(initial=0) <= 1, f"{what}: codes differ from the oracle by {d2.max()} codes"
     return q_ref, s_ref
 
 

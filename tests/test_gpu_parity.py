@@ -93,25 +93,39 @@ def check_fused(orc, got, ref, dtype, quant):
         if got["y"] is not None:
             assert_fp8(orc, got["q"], got["scale"], y_for_q, dtype, ref)
         else:
-            # no mirror: the kernel's y is not visible, so compare with the oracle's own y;
-            # equal-scale rows must agree within one code
+            # no mirror: the kernel's y is not visible, so compare with the oracle's own y.
+            # Every row's scale is within one 16-bit ulp of amax of the oracle's (the y bar at
+            # the amax element), almost every row's scale is equal, and every code is within
+            # one code: a scale off by 2^-7 and a y off by one ulp move a quotient by less than
+            # half an E4M3 step, so at most one rounding boundary is crossed.
+            from gpu_helpers import code_ordinal
+            s_g, s_r = got["scale"].astype(np.float64), ref["scale"].astype(np.float64)
+            tol = 2.0 ** -7 if dtype == "bf16" else 2.0 ** -10
+            assert np.all(np.abs(s_g - s_r) <= tol * s_r * 1.0001), "scale beyond one ulp of amax of the oracle's"
             same = got["scale"] == ref["scale"]
             assert same.mean() > 0.99
-            from gpu_helpers import code_ordinal
-            d = np.abs(code_ordinal(got["q"][same]) - code_ordinal(ref["q"][same]))
-            assert d.max(initial=0) <= 1
+            d = np.abs(code_ordinal(got["q"]) - code_ordinal(ref["q"]))
+            assert d.max(initial=0) <= 1, f"codes differ from the oracle's by {d.max()} codes"
 
 
 WORKLOADS = synth.all_fused()
 
 
 @pytest.mark.parametrize("wl", WORKLOADS, ids=[w.name for w in WORKLOADS])
-def test_fused_workloads_full_size(ctx, dev, orc, wl):
+def test_fused_workloads_full_size(ctx, dev, orc, wl, record_property):
     inp = wl.inputs()
     got = run_fused(ctx, dev, inp, wl.dtype, wl.gemma, wl.quant, wl.mirror)
     ref = oracle_fused(orc, inp, wl.dtype, wl.gemma, wl.quant)
     check_fused(orc, got, ref, wl.dtype, wl.quant)
     assert got["variant"].startswith("fused_")
+    if wl.quant:
+        # rows whose scale takes the one-ulp-of-amax allowance (the kernel's y at the row's
+        # largest element one ulp from the oracle's): counted, and bounded at 1 % of rows so
+        # that a drift in the norm arithmetic shows up as a number
+        n_diff = int(np.count_nonzero(got["scale"] != ref["scale"]))
+        record_property("scale_rows_one_ulp_of_amax", f"{n_diff} of {wl.m}")
+        print(f"\n{wl.name}: {n_diff} of {wl.m} rows with a scale one ulp of amax from the oracle's")
+        assert n_diff <= 0.01 * wl.m
 
 
 # shape list of the fused AR + RMSNorm test command on the gfx1250 page

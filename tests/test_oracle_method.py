@@ -295,6 +295,45 @@ def test_quant_properties(orc, dtype):
     assert np.array_equal(qn[nz], q[nz] ^ np.uint8(0x80))
 
 
+def test_quant_tiny_rows_and_groups(orc):
+    """Rows and groups of tiny bf16 magnitude (maxima 2^-133 .. 2^-118), where the binary32
+    scale amax / 448 is subnormal: the scale is still the binary32 quotient with gradual
+    underflow, and each code the E4M3 rounding of the binary32 quotient y / scale.  Expected
+    values from numpy's binary32 arithmetic and torch's E4M3 cast (saturation at 448 applied
+    first, as the format's satfinite conversion does), not from the oracle."""
+    g = np.random.default_rng(21)
+    m, h = 64, 96
+    ks = -133 + (np.arange(m) % 16)
+    vals = (g.standard_normal((m, h)) * 2.0 ** ks[:, None]).astype(np.float32)
+    y = synth.bits(torch.from_numpy(vals).to(torch.bfloat16))
+    y[5, :] = 0                                          # an all-zero row among them
+    yf = _dec(y, "bf16")
+    amax = np.abs(yf).max(axis=1).astype(np.float32)
+    sc_exp = amax / np.float32(448.0)
+    assert np.count_nonzero((sc_exp > 0) & (sc_exp < np.float32(2.0 ** -126))) > 40   # subnormal scales
+    with np.errstate(divide="ignore", invalid="ignore"):
+        quo = np.where(amax[:, None] > 0, yf / sc_exp[:, None], np.float32(0.0)).astype(np.float32)
+    q_exp = torch.from_numpy(np.clip(quo, -448.0, 448.0)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    q, sc = orc.per_token_quant(y, "bf16")
+    assert np.array_equal(sc.view(np.uint32), sc_exp.view(np.uint32))
+    assert np.array_equal(q, q_exp)
+    assert not np.any((q & 0x7F) == 0x7F)               # no NaN code
+    # per group: groups of 16 with tiny and normal groups side by side in one row
+    yg = y.copy().reshape(m, h // 16, 16)
+    big = synth.bits(torch.from_numpy(g.standard_normal((m, h // 16, 16)).astype(np.float32)).to(torch.bfloat16))
+    yg[:, 1::2, :] = big[:, 1::2, :]
+    yg = yg.reshape(m, h)
+    qg, scg = orc.per_group_quant(yg, 16, "bf16")
+    yv = _dec(yg, "bf16").reshape(m, h // 16, 16)
+    am = np.abs(yv).max(axis=2).astype(np.float32)
+    s_exp = am / np.float32(448.0)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        qq = np.where(am[:, :, None] > 0, yv / s_exp[:, :, None], np.float32(0.0)).astype(np.float32)
+    qg_exp = torch.from_numpy(np.clip(qq, -448.0, 448.0)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(scg.view(np.uint32), s_exp.reshape(m, -1).view(np.uint32))
+    assert np.array_equal(qg, qg_exp.reshape(m, h))
+
+
 # ---------------------------------------------------------------------------
 # options: no normalisation (all-reduce + per-token FP8) and binary32 output
 # ---------------------------------------------------------------------------
