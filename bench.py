@@ -4,11 +4,14 @@
 Metric: microseconds per call under CUDA-graph replay, and the achieved HBM bandwidth of
 the fused kernel as a fraction of the measured GB300 copy bandwidth.
 
-Headline workload: N=4 bf16 partials of 2800 x 6144, residual in/out, gemma (1 + w)
-RMSNorm, per-token FP8 E4M3 codes with fp32 scales and the bf16 mirror, i.e. every step of
-the path in one call.  A "step" is one replay of a CUDA graph holding `calls_per_step`
-calls that rotate over buffer sets larger than L2 together, the methodology of the pages'
-benchmarks (k calls captured per graph, replays timed with CUDA events).
+Headline workload: the largest single-GPU configuration, N=8 bf16 partials of 4096 x 6144
+(48 MiB each), residual in/out, plain RMSNorm, bf16 output (554 MB moved per call).  The
+gemma + per-token FP8 + bf16 mirror call on N=4, 2800 x 6144 (every step of the path in
+one call) is timed the same way as a second named entry.  A "step" is one replay of a CUDA
+graph holding `calls_per_step` calls that rotate over buffer sets larger than L2 together,
+the methodology of the pages' benchmarks (k calls captured per graph, replays timed with
+CUDA events).  The JSON line ends with a compact per-configuration summary (every workload
+of the five configurations: us/call HBM-cold and L2-warm, GB/s, fraction of peak).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -18,6 +21,7 @@ exchange between GPUs); rank 0 prints one JSON line.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -31,7 +35,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-HEADLINE = "n4_m2800_h6144_bf16_gemma_fp8"
+HEADLINE = "n8_m4096_h6144_bf16_plain"
+SECOND = "n4_m2800_h6144_bf16_gemma_fp8"
 METRIC = "us/call (CUDA-graph replay) and achieved HBM GB/s, fused reduce+RMSNorm"
 UNIT = "us/call"
 SMI_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -390,19 +395,35 @@ def e2e_copy_engines(ctx, wl, steps: int, dev):
 # the oracle on the host cores (CPU baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_sample_us(wl, rows: int):
-    """Time the oracle on the first `rows` rows of the workload; returns (us per full call, rows)."""
-    import oracle
-    from tensor_all_reduce_gb300 import synth
-    rows = max(1, min(rows, wl.m))
-    inp = synth.fused_inputs(wl.n, rows, wl.h, wl.dtype, seed=wl.seed, gemma=wl.gemma, residual=wl.residual)
-    orc = oracle.get()
-    args = ([synth.bits(p) for p in inp["partials"]], synth.bits(inp["residual"]), synth.bits(inp["weight"]),
-            1e-6, wl.gemma, wl.quant, wl.dtype)
+class OracleInputs:
+    """A workload's inputs in the oracle's storage convention, drawn once (outside any timing)."""
+
+    def __init__(self, wl):
+        from tensor_all_reduce_gb300 import synth
+        self.wl = wl
+        inp = wl.inputs()
+        self.parts = [synth.bits(p) for p in inp["partials"]]
+        self.res = synth.bits(inp["residual"]) if inp["residual"] is not None else None
+        self.w = None if wl.skip_norm else synth.bits(inp["weight"])
+
+    def call(self, orc, a: int = 0, b: int | None = None):
+        """One oracle call on rows [a, b) (the whole call by default)."""
+        wl = self.wl
+        b = wl.m if b is None else b
+        parts = [p[a:b] for p in self.parts]
+        res = None if self.res is None else self.res[a:b]
+        if wl.skip_norm or wl.out_fp32 or wl.group:
+            orc.fused_ex(parts, res, self.w, 1e-6, wl.gemma, wl.quant, wl.dtype, skip_norm=wl.skip_norm,
+                         out_fp32=wl.out_fp32, group=wl.group)
+        else:
+            orc.fused(parts, res, self.w, 1e-6, wl.gemma, wl.quant, wl.dtype)
+
+
+def timed_oracle_s(inputs, orc, rows: int) -> float:
+    """Seconds of one oracle call on the first `rows` rows."""
     t = time.perf_counter()
-    orc.fused(*args)
-    dt = time.perf_counter() - t
-    return dt * 1e6 * (wl.m / rows), rows
+    inputs.call(orc, 0, rows)
+    return time.perf_counter() - t
 
 
 def cpu_model() -> str:
@@ -426,85 +447,108 @@ def host_cores() -> int:
     return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
 
-def oracle_all_cores_us(wl, seconds: float = 4.0, runs: int = 3):
-    """Rows partitioned over every host core: each thread runs the same serial oracle on its own
-    contiguous block of rows (rows are independent; the C call releases the GIL).  Returns
-    (us per full call, threads, rows per run)."""
-    import oracle
+def rows_for_budget(wl, per_call_s: float, calls: int, budget_s: float) -> int:
+    """Whole calls when `calls` of them fit in the budget, else the most rows that do."""
+    if per_call_s * calls <= budget_s:
+        return wl.m
+    return max(1, min(wl.m, int(budget_s / calls / (per_call_s / wl.m))))
+
+
+def oracle_all_cores_us(inputs, orc, runs: int = 3):
+    """Whole calls with the rows partitioned over every host core: each thread runs the same
+    serial oracle on its own contiguous block of rows (rows are independent; the C call
+    releases the GIL).  Returns (us per call, threads)."""
     from concurrent.futures import ThreadPoolExecutor
-    from tensor_all_reduce_gb300 import synth
     cores = host_cores()
-    us1, _ = oracle_sample_us(wl, 16)
-    per_row_s = us1 / 1e6 / wl.m
-    rows = max(cores, min(wl.m, int(seconds / runs * cores / per_row_s)))
-    inp = synth.fused_inputs(wl.n, rows, wl.h, wl.dtype, seed=wl.seed, gemma=wl.gemma, residual=wl.residual)
-    parts = [synth.bits(p) for p in inp["partials"]]
-    res = synth.bits(inp["residual"]) if inp["residual"] is not None else None
-    w = synth.bits(inp["weight"])
-    orc = oracle.get()
-    bounds = [rows * k // cores for k in range(cores + 1)]
+    m = inputs.wl.m
+    bounds = [m * k // cores for k in range(cores + 1)]
 
     def block(k):
-        a, b = bounds[k], bounds[k + 1]
-        if b > a:
-            orc.fused([p[a:b] for p in parts], None if res is None else res[a:b], w, 1e-6,
-                      wl.gemma, wl.quant, wl.dtype)
+        if bounds[k + 1] > bounds[k]:
+            inputs.call(orc, bounds[k], bounds[k + 1])
 
     samples = []
     with ThreadPoolExecutor(cores) as ex:
         for _ in range(runs):
             t = time.perf_counter()
             list(ex.map(block, range(cores)))
-            samples.append((time.perf_counter() - t) * 1e6 * (wl.m / rows))
-    return statistics.median(samples), cores, rows
+            samples.append((time.perf_counter() - t) * 1e6)
+    return statistics.median(samples), cores
 
 
-def cpu_baseline(wl, seconds: float = 12.0, runs: int = 5):
-    """Serial oracle (one thread, pinned to one core), timed on a bounded sample of the
-    workload's rows; beside it the same oracle with the rows partitioned over all host cores."""
-    us1, rows = oracle_sample_us(wl, 16)                 # size the sample
-    per_row_s = us1 / 1e6 / wl.m
-    rows = max(16, min(wl.m, int(seconds / runs / per_row_s)))
+def cpu_baseline(wl, budget_s: float = 30.0, runs: int = 3):
+    """The serial oracle (one thread, pinned to one core) on whole calls of the workload,
+    median of `runs` (fewer whole calls, or a row sample, if they would exceed the budget);
+    beside it the same oracle with the rows partitioned over all host cores."""
+    import oracle
+    orc = oracle.get()
+    inputs = OracleInputs(wl)
+    probe_rows = min(wl.m, 16)
+    per_call_s = timed_oracle_s(inputs, orc, probe_rows) * wl.m / probe_rows
+    runs = max(1, min(runs, int(budget_s / max(per_call_s, 1e-9))))
+    rows = rows_for_budget(wl, per_call_s, runs, budget_s)
     pinned = hasattr(os, "sched_setaffinity")
     if pinned:
         cpus = os.sched_getaffinity(0)
         os.sched_setaffinity(0, {min(cpus)})            # this thread only, restored below
     try:
-        samples = [oracle_sample_us(wl, rows)[0] for _ in range(runs)]
+        samples = [timed_oracle_s(inputs, orc, rows) * 1e6 * wl.m / rows for _ in range(runs)]
     finally:
         if pinned:
             os.sched_setaffinity(0, cpus)
-    mt_us, cores, mt_rows = oracle_all_cores_us(wl)
+    mt_us, cores = oracle_all_cores_us(inputs, orc)
     value = statistics.median(samples)
     fp = wl.algorithmic_bytes()
-    return {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "cpu": cpu_model(),
+    what = "whole calls" if rows == wl.m else f"{rows} of {wl.m} rows per run, scaled to a full call"
+    return {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "cpu": cpu_model(),
             "gbs": round(fp / (value * 1e-6) / 1e9, 4),
-            "sample": f"serial C oracle on {rows} of {wl.m} rows, one thread pinned to one core, median of "
-                      f"{runs} runs, scaled to a full call",
+            "sample": f"serial C oracle, {what}, one thread pinned to one core, median of {runs} runs",
             "all_cores": {"value": round(mt_us, 3), "unit": UNIT, "cores": cores,
                           "gbs": round(fp / (mt_us * 1e-6) / 1e9, 4),
-                          "sample": f"the same oracle, {mt_rows} of {wl.m} rows split in {cores} row blocks "
-                                    f"over {cores} threads, median of 3 runs, scaled to a full call"}}
+                          "sample": f"the same oracle on whole calls, the rows split in {cores} contiguous blocks "
+                                    f"over {cores} threads, median of 3 runs"}}
+
+
+def workload_config(wl, world: int) -> dict:
+    """The `config` object of both arms' JSON lines: what the workload is."""
+    fp = wl.algorithmic_bytes()
+    cfg = {"workload": wl.name, "n_partials": wl.n, "m": wl.m, "h": wl.h, "dtype": wl.dtype, "gemma": wl.gemma,
+           "residual": wl.residual, "fp8_per_token": wl.quant and not wl.group, "bf16_mirror": wl.quant and wl.mirror,
+           "bytes_per_call": fp,
+           "l2": f"inputs larger than L2 ({fp / 1e6:.0f} MB per call against a 126 MiB L2), buffer sets "
+                 f"rotating over at least three times L2",
+           "parallelism": "replicas" if world > 1 else "single GPU"}
+    return cfg
 
 
 def run_reference(args, world, rank):
+    """The reference arm: the serial oracle (the pages hold no installable code) on the host
+    cores, on the same workload, metric and unit.  Each step is one whole call when warm-up and
+    steps fit in about two and a half minutes, else the same row sample every step (the value is
+    then scaled to a full call); ms_per_step is the time a step actually took."""
+    import oracle
     from tensor_all_reduce_gb300 import synth
     if rank != 0:
         return 0
     wl = synth.by_name(args.workload)
-    us1, _ = oracle_sample_us(wl, 8)
-    # size each step so that warm-up + steps stay within about two minutes
-    budget_s = min(120.0, 1.0 * (args.steps + args.warmup))
-    rows = max(1, min(wl.m, int(budget_s / (args.steps + args.warmup) / (us1 / 1e6 / wl.m))))
+    orc = oracle.get()
+    inputs = OracleInputs(wl)
+    probe_rows = min(wl.m, 16)
+    per_call_s = timed_oracle_s(inputs, orc, probe_rows) * wl.m / probe_rows
+    rows = rows_for_budget(wl, per_call_s, args.steps + args.warmup, 150.0)
     for _ in range(args.warmup):
-        oracle_sample_us(wl, rows)
-    times = [oracle_sample_us(wl, rows)[0] for _ in range(args.steps)]
-    value = statistics.median(times)
-    sample = f"serial C oracle on {rows} of {wl.m} rows per step, scaled to a full call; median of {args.steps} steps"
+        timed_oracle_s(inputs, orc, rows)
+    step_s = [timed_oracle_s(inputs, orc, rows) for _ in range(args.steps)]
+    value = statistics.median(step_s) * 1e6 * wl.m / rows
+    if rows == wl.m:
+        sample = f"serial C oracle, one whole call per step, median of {args.steps} steps"
+    else:
+        sample = (f"serial C oracle on the first {rows} of {wl.m} rows per step, median of {args.steps} steps, "
+                  f"scaled to a full call")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sum(times) / len(times) / 1000, 3),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sum(step_s) / len(step_s) * 1e3, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype,
-            "data": "synthetic", "config": {"workload": wl.name, "n_partials": wl.n, "m": wl.m, "h": wl.h},
+            "data": "synthetic", "config": workload_config(wl, world), "rows_per_step": rows,
             "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle", "cpu": cpu_model(),
                              "sample": sample},
             "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -516,31 +560,60 @@ def run_reference(args, world, rank):
 # main
 # ---------------------------------------------------------------------------
 
-def sweep(ctx, dev, l2, peak):
-    """Every workload family once (short): us/call cold (rotating sets) and warm (one set)."""
+def time_workload(ctx, dev, wl, l2, peak, steps: int = 5, warmup: int = 2):
+    """us/call of one workload, HBM-cold (buffer sets rotating over three times L2) and
+    L2-warm (the same buffers every call), with GB/s and the fraction of peak."""
     import torch
     from tensor_all_reduce_gb300 import synth
-    out = []
-    for wl in synth.all_fused() + synth.options() + synth.reduce_only() + synth.reduce_large():
-        fused = isinstance(wl, synth.FusedWorkload)
-        fp = wl.algorithmic_bytes()
-        R = rotation_sets(fp, l2)
-        calls = max(64, R)
-        sets = (FusedSets if fused else ReduceSets)(wl, R, dev)
-        ms, *_ = time_graph(sets, ctx, calls, steps=5, warmup=2, world=1)
-        cold = ms * 1000 / (5 * calls)
-        variant = ctx.last_variant
-        del sets
-        torch.cuda.empty_cache()
-        sets = (FusedSets if fused else ReduceSets)(wl, 1, dev)
-        ms, *_ = time_graph(sets, ctx, 64, steps=5, warmup=2, world=1)
-        warm = ms * 1000 / (5 * 64)
-        del sets
-        torch.cuda.empty_cache()
-        gbs = fp / (cold * 1e-6) / 1e9
-        out.append({"workload": wl.name, "variant": variant, "us_per_call_cold": round(cold, 3),
-                    "us_per_call_l2_warm": round(warm, 3), "bytes_per_call": fp, "gbs_cold": round(gbs, 1),
-                    "frac_of_peak_cold": round(gbs / peak, 4), "rotation_sets": R})
+    fused = isinstance(wl, synth.FusedWorkload)
+    fp = wl.algorithmic_bytes()
+    R = rotation_sets(fp, l2)
+    calls = max(64, R)
+    sets = (FusedSets if fused else ReduceSets)(wl, R, dev)
+    ms, *_ = time_graph(sets, ctx, calls, steps=steps, warmup=warmup, world=1)
+    cold = ms * 1000 / (steps * calls)
+    variant = ctx.last_variant
+    del sets
+    torch.cuda.empty_cache()
+    sets = (FusedSets if fused else ReduceSets)(wl, 1, dev)
+    ms, *_ = time_graph(sets, ctx, 64, steps=steps, warmup=warmup, world=1)
+    warm = ms * 1000 / (steps * 64)
+    del sets
+    torch.cuda.empty_cache()
+    gbs = fp / (cold * 1e-6) / 1e9
+    return {"workload": wl.name, "variant": variant, "us_per_call_cold": round(cold, 3),
+            "us_per_call_l2_warm": round(warm, 3), "bytes_per_call": fp, "gbs_cold": round(gbs, 1),
+            "frac_of_peak_cold": round(gbs / peak, 4), "rotation_sets": R}
+
+
+def config_workloads():
+    """Every workload of the five configurations, in order: C1 (N=4, 16 x 6144 plain), C2
+    (reduce-only 1023/1024/1025 x 512, fp16 and fp32), C3 (decode 1/16/64/256 x 6144), C4
+    (gemma + FP8 + mirror at 1024/2800 x 6144 and 1024 x 7168), C5 (N=8, 4096 x 6144)."""
+    from tensor_all_reduce_gb300 import synth
+    return ([("C1", w) for w in synth.small_fused()] + [("C2", w) for w in synth.reduce_only()]
+            + [("C3", w) for w in synth.decode_sweep()] + [("C4", w) for w in synth.gemma_fp8()]
+            + [("C5", w) for w in synth.large_m()])
+
+
+def configs_summary(ctx, dev, l2, peak):
+    """Compact per-configuration table: {"C4 n4_m2800_h6144_bf16_gemma_fp8": [variant, us cold,
+    us L2-warm, GB/s cold, fraction of peak cold], ...}."""
+    out = {}
+    for tag, wl in config_workloads():
+        e = time_workload(ctx, dev, wl, l2, peak)
+        out[f"{tag} {wl.name}"] = [e["variant"], e["us_per_call_cold"], e["us_per_call_l2_warm"], e["gbs_cold"],
+                                   e["frac_of_peak_cold"]]
+    return out
+
+
+def sweep(ctx, dev, l2, peak):
+    """The workloads outside the five configurations (wide rows, the further forms of the fused
+    call, the large plain sums) and 8 decode calls batched against 8 launches."""
+    import torch
+    from tensor_all_reduce_gb300 import synth
+    out = [time_workload(ctx, dev, wl, l2, peak)
+           for wl in synth.wide_rows() + synth.row_kernel_shape() + synth.options() + synth.reduce_large()]
     # 8 independent decode calls (16 x 6144 each): one batched launch against 8 launches
     wl = synth.FusedWorkload("n4_m16_h6144_bf16_decode", 4, 16, 6144, seed=1236)
     k = 8
@@ -562,6 +635,84 @@ def sweep(ctx, dev, l2, peak):
     return out
 
 
+def run_env(ctx, dev) -> dict:
+    """Facts about the run: the device, the CUDA runtime and driver, the library's hash, the host."""
+    import torch
+    import tensor_all_reduce_gb300 as tar
+    props = torch.cuda.get_device_properties(dev)
+    env = {"device": props.name, "sm_count": ctx.info(tar.AR_INFO_SM_COUNT), "l2_bytes": ctx.info(tar.AR_INFO_L2_BYTES),
+           "hbm_bytes": props.total_memory, "cc": f"{props.major}.{props.minor}", "torch": torch.__version__,
+           "cuda_runtime_torch": torch.version.cuda, "host_cores": host_cores(), "host_cpu": cpu_model()}
+    try:
+        rt, drv = ctypes.c_int(), ctypes.c_int()
+        cudart = ctypes.CDLL("libcudart.so.13") if os.path.exists("/usr/local/cuda/lib64/libcudart.so.13") else None
+        if cudart is not None and cudart.cudaRuntimeGetVersion(ctypes.byref(rt)) == 0:
+            env["cuda_runtime"] = rt.value
+        if cudart is not None and cudart.cudaDriverGetVersion(ctypes.byref(drv)) == 0:
+            env["cuda_driver"] = drv.value
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=driver_version", "--format=csv,noheader", "-i",
+                              str(dev.index or 0)], capture_output=True, text=True, timeout=20)
+        if out.returncode == 0:
+            env["nvidia_driver"] = out.stdout.strip()
+    except (OSError, subprocess.TimeoutExpired):
+        pass
+    with open(tar.LIB_PATH, "rb") as f:
+        env["libar_sha256"] = hashlib.sha256(f.read()).hexdigest()
+    env["kernel_src_hash"] = kernel_source_hash()
+    return env
+
+
+def timed_headline(ctx, dev, wl, l2, args, world, rank):
+    """The CUDA-graph measurement of one workload as the bench line reports it."""
+    import torch
+    fp = wl.algorithmic_bytes()
+    R = max(2, rotation_sets(fp, l2, cap=64))
+    calls = max(args.calls_per_step, R)
+    sets = FusedSets(wl, R, dev)
+    sampler = ClockSampler(dev.index or 0) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    elapsed_ms, t0, t1, step_ms = time_graph(sets, ctx, calls, args.steps, args.warmup, world)
+    clocks = sampler.stop(t0, t1) if sampler else None
+    variant = ctx.last_variant
+    del sets
+    torch.cuda.empty_cache()
+    return {"elapsed_ms": elapsed_ms, "step_ms": step_ms, "clocks": clocks, "variant": variant, "R": R,
+            "calls": calls, "fp": fp}
+
+
+def run_case(args, dev):
+    """--case NAME: `case_calls` eager calls of one named workload (fused or plain reduce) over
+    buffer sets rotating across three times L2, timed with CUDA events; prints one JSON line.
+    A short, self-contained run for profiling one kernel launch at a time."""
+    import torch
+    import tensor_all_reduce_gb300 as tar
+    from tensor_all_reduce_gb300 import synth
+    wl = synth.by_name(args.case)
+    with tar.Context(dev.index or 0) as ctx:
+        l2 = ctx.info(tar.AR_INFO_L2_BYTES)
+        fused = isinstance(wl, synth.FusedWorkload)
+        R = rotation_sets(wl.algorithmic_bytes(), l2, cap=64)
+        sets = (FusedSets if fused else ReduceSets)(wl, R, dev)
+        for i in range(args.warmup):
+            sets.call(ctx, i)
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for i in range(args.case_calls):
+            sets.call(ctx, args.warmup + i)
+        end.record()
+        end.synchronize()
+        us = start.elapsed_time(end) * 1000.0 / max(args.case_calls, 1)
+        print(json.dumps({"case": wl.name, "variant": ctx.last_variant, "calls": args.case_calls, "warmup": args.warmup,
+                          "buffer_sets": R, "us_per_call_eager": round(us, 3),
+                          "bytes_per_call": wl.algorithmic_bytes()}), flush=True)
+    return 0
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
@@ -570,9 +721,11 @@ def main(argv=None):
     p.add_argument("--impl", choices=("ours", "reference"), default="ours")
     p.add_argument("--workload", default=HEADLINE)
     p.add_argument("--calls-per-step", type=int, default=500)
-    p.add_argument("--no-sweep", action="store_true", help="skip the per-workload sweep")
+    p.add_argument("--no-sweep", action="store_true", help="skip the per-configuration summary and the sweep")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--case", default=None, help="run only `--case-calls` eager calls of this workload")
+    p.add_argument("--case-calls", type=int, default=3)
     args = p.parse_args(argv)
     world, rank, local = dist_env()
     if args.impl == "reference":
@@ -586,6 +739,10 @@ def main(argv=None):
         return 1
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.case:
+        import __graft_entry__
+        __graft_entry__.build()
+        return run_case(args, dev)
     init_dist(world, "nccl")
     import __graft_entry__
     if rank == 0:
@@ -595,46 +752,49 @@ def main(argv=None):
     l2 = ctx.info(tar.AR_INFO_L2_BYTES)
     peak, peak_kind = measured_peaks()
     wl = synth.by_name(args.workload)
-    fp = wl.algorithmic_bytes()
-    R = rotation_sets(fp, l2, cap=64)
-    calls = max(args.calls_per_step, R)
-    sets = FusedSets(wl, R, dev)
 
-    sampler = ClockSampler(local) if rank == 0 else None
-    if sampler:
-        sampler.start()
-    elapsed_ms, t0, t1, step_ms = time_graph(sets, ctx, calls, args.steps, args.warmup, world)
-    clocks = sampler.stop(t0, t1) if sampler else None
-    variant = ctx.last_variant
-    max_ms = max_over_ranks(elapsed_ms, world, dev)
+    hl = timed_headline(ctx, dev, wl, l2, args, world, rank)
+    fp, calls = hl["fp"], hl["calls"]
+    max_ms = max_over_ranks(hl["elapsed_ms"], world, dev)
     launches = args.steps * calls
     value = job_us_per_call(max_ms, launches, world)
-    per_launch_us = elapsed_ms * 1000.0 / launches          # this rank's average launch duration
+    per_launch_us = hl["elapsed_ms"] * 1000.0 / launches    # this rank's average launch duration
     achieved = fp / (per_launch_us * 1e-6) / 1e9
-    del sets
-    torch.cuda.empty_cache()
 
     e2e_us, h2d, d2h = e2e_fused(ctx, wl, args.e2e_steps, dev)
     e2e_us = max_over_ranks(e2e_us, world, dev) / world
     copy_us = e2e_copy_engines(ctx, wl, args.e2e_steps, dev)
 
+    second = None
+    if args.workload != SECOND:
+        wl2 = synth.by_name(SECOND)
+        s2 = timed_headline(ctx, dev, wl2, l2, args, 1, 1)
+        us2 = s2["elapsed_ms"] * 1000.0 / (args.steps * s2["calls"])
+        gbs2 = s2["fp"] / (us2 * 1e-6) / 1e9
+        second = {"workload": wl2.name, "value": round(us2, 3), "unit": UNIT, "variant": s2["variant"],
+                  "achieved_gbs": round(gbs2, 1), "frac": round(gbs2 / peak, 4), "bytes_per_call": s2["fp"],
+                  "traffic": recorded_traffic(wl2.name), "calls_per_step": s2["calls"], "buffer_sets": s2["R"],
+                  "per_step_median": round(statistics.median(s2["step_ms"]) * 1000.0 / s2["calls"], 3)}
+
     extra = {}
     if rank == 0 and not args.no_sweep:
         extra["sweep"] = sweep(ctx, dev, l2, peak)
+        extra["configs"] = configs_summary(ctx, dev, l2, peak)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(wl)
+    env = run_env(ctx, dev) if rank == 0 else None
     ctx.close()
     if rank == 0:
+        step_ms = hl["step_ms"]
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4), "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-            "config": {"workload": wl.name, "n_partials": wl.n, "m": wl.m, "h": wl.h, "gemma": wl.gemma,
-                       "fp8_per_token": wl.quant, "bf16_mirror": wl.mirror, "calls_per_step": calls,
-                       "buffer_sets": R, "l2": f"inputs larger than L2 ({fp / 1e6:.0f} MB per call vs "
-                                                f"{l2 / 1e6:.0f} MB L2), {R} rotating buffer sets",
-                       "parallelism": "replicas" if world > 1 else "single GPU", "variant": variant},
+            "config": workload_config(wl, world),
+            "timing": {"calls_per_step": calls, "buffer_sets": hl["R"], "variant": hl["variant"],
+                       "method": "CUDA-graph replays of calls_per_step calls rotating over buffer_sets sets, "
+                                 "CUDA events on the replaying stream"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": recorded_traffic(wl.name),
                          "peak_kind": peak_kind, "algorithmic_bytes_per_launch": fp},
@@ -648,11 +808,17 @@ def main(argv=None):
                          "max": round(max(step_ms) * 1000.0 / calls, 3), "unit": UNIT,
                          "note": "rank 0's replays one by one (CUDA events between replays)"},
             "gpu_launches": launches,
-            "clocks": clocks,
+            "clocks": hl["clocks"],
+            "env": env,
         }
         if cpu is not None:
             line["cpu_baseline"] = cpu
-        line.update(extra)
+        if second is not None:
+            line["second"] = second
+        if "sweep" in extra:
+            line["sweep"] = extra["sweep"]
+            line["configs_fields"] = ["variant", "us_cold", "us_l2_warm", "gbs_cold", "frac_of_peak_cold"]
+            line["configs"] = extra["configs"]          # last: the end of the line is what a log tail keeps
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -280,10 +280,14 @@ typedef enum {
                                 complete before it reads memory); 0: ordinary stream order */
   AR_OPT_WAIT_CYCLES = 6,    /* bound of one staged-kernel wait in SM clock cycles (1e3..8e9);
                                 0 (the default): 2e9, about a second */
-  AR_OPT_TEST_STALL = 7      /* test hook, 0 (the default) or 1: the staged kernels arm each CTA's
+  AR_OPT_TEST_STALL = 7,     /* test hook, 0 (the default) or 1: the staged kernels arm each CTA's
                                 first stage without issuing its copies, so that wait runs out and
                                 the call ends early with code 1 in the status word (exercises the
                                 failure path; outputs are then incomplete) */
+  AR_OPT_L2_PREFETCH = 8     /* 1 (the default): the kernels on device memory prefetch their first
+                                rows (or tile) of input into L2 before waiting for the previous
+                                kernel on the stream, so those reads overlap its tail; 0: off.
+                                Results are the same either way */
 } ar_option;
 ar_status ar_set_option(ar_ctx* ctx, ar_option opt, int64_t value);
 

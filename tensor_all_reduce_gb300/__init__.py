@@ -44,6 +44,7 @@ AR_OPT_STAGES = 4
 AR_OPT_PDL = 5
 AR_OPT_WAIT_CYCLES = 6
 AR_OPT_TEST_STALL = 7
+AR_OPT_L2_PREFETCH = 8
 VARIANT_AUTO, VARIANT_ROW, VARIANT_CLUSTER, VARIANT_STAGED, VARIANT_SCALAR = 0, 1, 2, 3, 4
 
 AR_INFO_SM_COUNT = 0

@@ -30,6 +30,7 @@ struct ar_ctx {
   int pdl;               // launch with programmatic stream serialisation
   long long wait_cycles; // bound of one staged-kernel wait (0: about a second)
   int test_stall;        // test hook: make the staged kernel's first waits run out
+  int prefetch;          // warm L2 with the first inputs before the grid-dependency wait
   const char* last_variant;
   char last_error[256];
 };
@@ -99,6 +100,32 @@ ar_status launch(ar_ctx* ctx, const void* fn, unsigned grid, unsigned block, int
 }  // namespace
 
 namespace ar {
+void fill_fused_params(FusedParams& p, const ar_fused_args& a, int chunk, int csize) {
+  memset(&p, 0, sizeof(p));
+  for (int r = 0; r < a.n; ++r) p.x[r] = a.partials[r];
+  p.res_in = a.residual_in;
+  p.res_out = a.residual_out;
+  p.w = a.weight;
+  p.out = a.out;
+  p.q = static_cast<uint8_t*>(a.q_out);
+  p.scale = a.scale_out;
+  p.m = a.m;
+  p.h = (int)a.h;
+  p.row_packs = (int)((a.h + 7) / 8);
+  p.chunk_packs = chunk;
+  p.csize = csize;
+  p.eps = a.eps;
+  p.inv_h = (float)(1.0 / (double)a.h);
+  p.gemma = a.gemma != 0;
+  p.skip_norm = a.skip_norm != 0;
+  p.out_f32 = a.out_fp32 != 0 && a.out != nullptr;
+  const bool per_group = a.quant == AR_QUANT_FP8_E4M3_PER_GROUP;
+  p.group_lanes = per_group ? a.group_size / 8 : 0;
+  p.ngroups = per_group ? (int)(a.h / a.group_size) : 0;
+  p.ld_in = a.ld_in ? a.ld_in : a.h;
+  p.ld_out = a.ld_out ? a.ld_out : a.h;
+}
+
 int fused_kernel_list(const void** out, int cap) {
   int k = 0;
   for (int dt = 0; dt < 2; ++dt)
@@ -179,6 +206,7 @@ ar_status ar_init(ar_ctx** out, int device, unsigned flags) {
   ctx->last_variant = "none";
   ctx->max_cluster = 8;
   ctx->pdl = 1;
+  ctx->prefetch = 1;
 
   DeviceGuard g(device);
   // Load every kernel now (lazy module loading would otherwise do it on first launch,
@@ -312,6 +340,10 @@ ar_status ar_set_option(ar_ctx* ctx, ar_option opt, int64_t v) {
       if (v != 0 && v != 1) return AR_ERR_INVALID_ARG;
       ctx->test_stall = (int)v;
       return AR_OK;
+    case AR_OPT_L2_PREFETCH:
+      if (v != 0 && v != 1) return AR_ERR_INVALID_ARG;
+      ctx->prefetch = (int)v;
+      return AR_OK;
   }
   return AR_ERR_INVALID_ARG;
 }
@@ -366,6 +398,7 @@ ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int
   for (int r = 0; r < n; ++r) p.x[r] = partials[r];
   p.out = out;
   p.numel = numel;
+  p.prefetch = ctx->prefetch;
   bool vec = aligned(out, 16);
   for (int r = 0; r < n; ++r) vec = vec && aligned(partials[r], 16);
   if (ctx->force_variant == 4) vec = false;
@@ -529,28 +562,8 @@ static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, b
   const int rows_per_stage = a->n + (a->residual_in ? 1 : 0);
   // kernel parameters of the staged forms: `chunk` packs of each row per CTA, `cl` CTAs per row
   auto staged_params = [&](ar::FusedParams& p, ar::StagedParams& sp, int chunk, int cl, int stages) {
-    memset(&p, 0, sizeof(p));
-    for (int r = 0; r < a->n; ++r) p.x[r] = a->partials[r];
-    p.res_in = a->residual_in;
-    p.res_out = a->residual_out;
-    p.w = a->weight;
-    p.out = a->out;
-    p.q = static_cast<uint8_t*>(a->q_out);
-    p.scale = a->scale_out;
-    p.m = a->m;
-    p.h = (int)a->h;
-    p.row_packs = row_packs;
-    p.chunk_packs = chunk;
-    p.csize = cl;
-    p.eps = a->eps;
-    p.inv_h = (float)(1.0 / (double)a->h);
-    p.gemma = a->gemma != 0;
-    p.skip_norm = a->skip_norm != 0;
-    p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
-    p.group_lanes = per_group ? a->group_size / 8 : 0;
-    p.ngroups = per_group ? (int)(a->h / a->group_size) : 0;
-    p.ld_in = li;
-    p.ld_out = lo;
+    ar::fill_fused_params(p, *a, chunk, cl);
+    p.prefetch = ctx->prefetch;
     sp = ar::StagedParams{};
     sp.stages = stages;
     sp.row_bytes = chunk * 16;  // bytes of a row's chunk (a whole row without a cluster)
@@ -722,28 +735,8 @@ static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, b
   if (grid > 0x7FFFFFFFLL) return AR_ERR_UNSUPPORTED;
 
   ar::FusedParams p;
-  memset(&p, 0, sizeof(p));
-  for (int r = 0; r < a->n; ++r) p.x[r] = a->partials[r];
-  p.res_in = a->residual_in;
-  p.res_out = a->residual_out;
-  p.w = a->weight;
-  p.out = a->out;
-  p.q = static_cast<uint8_t*>(a->q_out);
-  p.scale = a->scale_out;
-  p.m = a->m;
-  p.h = (int)a->h;
-  p.row_packs = row_packs;
-  p.chunk_packs = chunk;
-  p.csize = csize;
-  p.eps = a->eps;
-  p.inv_h = (float)(1.0 / (double)a->h);
-  p.gemma = a->gemma != 0;
-  p.skip_norm = a->skip_norm != 0;
-  p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
-  p.group_lanes = per_group ? a->group_size / 8 : 0;
-  p.ngroups = per_group ? (int)(a->h / a->group_size) : 0;
-  p.ld_in = li;
-  p.ld_out = lo;
+  ar::fill_fused_params(p, *a, chunk, csize);
+  p.prefetch = host ? 0 : ctx->prefetch;  // bulk prefetches are used on device memory only
 
   const void* fn = a->dtype == AR_DTYPE_BF16 ? ar::fused_kernel_bf16(a->n, ppt, quant, vec)
                                              : ar::fused_kernel_f16(a->n, ppt, quant, vec);
@@ -914,28 +907,8 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_batch(ar_ctx* ctx, const ar_fused_a
   int64_t acc = 0;
   for (int i = 0; i < count; ++i) {
     const ar_fused_args& a = calls[i];
-    ar::FusedParams& p = bp.call[i];
-    for (int r = 0; r < a.n; ++r) p.x[r] = a.partials[r];
-    p.res_in = a.residual_in;
-    p.res_out = a.residual_out;
-    p.w = a.weight;
-    p.out = a.out;
-    p.q = static_cast<uint8_t*>(a.q_out);
-    p.scale = a.scale_out;
-    p.m = a.m;
-    p.h = (int)a.h;
-    p.row_packs = (int)(a.h / 8);
-    p.chunk_packs = p.row_packs;
-    p.csize = 1;
-    p.eps = a.eps;
-    p.inv_h = (float)(1.0 / (double)a.h);
-    p.gemma = a.gemma != 0;
-    p.skip_norm = a.skip_norm != 0;
-    p.out_f32 = a.out_fp32 != 0 && a.out != nullptr;
-    p.group_lanes = a.quant == AR_QUANT_FP8_E4M3_PER_GROUP ? a.group_size / 8 : 0;
-    p.ngroups = a.quant == AR_QUANT_FP8_E4M3_PER_GROUP ? (int)(a.h / a.group_size) : 0;
-    p.ld_in = a.ld_in;
-    p.ld_out = a.ld_out;
+    ar::fill_fused_params(bp.call[i], a, (int)(a.h / 8), 1);
+    bp.call[i].prefetch = ctx->prefetch;
     bp.row_start[i] = acc;
     acc += a.m;
   }

@@ -24,6 +24,7 @@ struct ReduceParams {
   int64_t npacks;      // full 16-byte packs
   int64_t numel;       // elements
   int64_t full_tiles;  // npacks / (blockDim * unroll)
+  int prefetch;        // 1: warm L2 with the first tile before waiting for the previous grid
 };
 
 struct FusedParams {
@@ -48,6 +49,7 @@ struct FusedParams {
   int ngroups;       // per-group FP8: groups per row, h / group
   int64_t ld_in;     // elements between row starts of the partials and residual_in (0: h)
   int64_t ld_out;    // elements between row starts of residual_out, out and q (0: h)
+  int prefetch;      // 1: warm L2 with the first rows' inputs before waiting for the previous grid
 };
 
 // ---------------------------------------------------------------------------
@@ -64,6 +66,16 @@ struct FusedParams {
 __device__ __forceinline__ void pdl_wait_and_release() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Bulk prefetch of `bytes` (a multiple of 16) at a 16-byte-aligned global address into L2.
+// It moves nothing into the kernel, so it may be issued before griddepcontrol.wait: a line
+// that the previous grid writes afterwards is updated in L2, the point of coherence of
+// global memory (SM stores write through to it), so later reads still see the new value.
+// Issued ahead of the wait, the first DRAM reads of a kernel overlap the tail of the one
+// before it on the stream.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // ---------------------------------------------------------------------------

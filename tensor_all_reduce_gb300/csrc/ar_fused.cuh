@@ -93,7 +93,6 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
   __shared__ float red_amax[32];
   __shared__ float slot_ss, slot_amax, bcast;
 
-  pdl_wait_and_release();
   const int csize = p.csize;
   const int crank = (int)(blockIdx.x % (unsigned)csize);  // == %cluster_ctarank for (csize,1,1) clusters
   const int64_t row = blockIdx.x / (unsigned)csize;
@@ -104,6 +103,18 @@ __global__ void __launch_bounds__(1024 / PPT) fused_kernel(const FusedParams p) 
   const int64_t row_i_end = row_i + p.h;
   const int64_t row_e = row * (p.ld_out ? p.ld_out : (int64_t)p.h);   // first output element of the row
   const int64_t row_end = row_e + p.h;         // one past the row's last output element
+
+  // this CTA's slice of the row into L2 while the previous grid may still run (see prefetch_l2)
+  if constexpr (VEC) {
+    if (p.prefetch && threadIdx.x == 0 && pk_end > pk_begin) {
+      const uint32_t bytes = (uint32_t)(pk_end - pk_begin) * 16u;
+      const int64_t e0 = row_i + (int64_t)pk_begin * 8;
+#pragma unroll
+      for (int r = 0; r < N; ++r) prefetch_l2(static_cast<const uint16_t*>(p.x[r]) + e0, bytes);
+      if (p.res_in != nullptr) prefetch_l2(static_cast<const uint16_t*>(p.res_in) + e0, bytes);
+    }
+  }
+  pdl_wait_and_release();
 
   // ---- phase 1: loads of every pack this thread owns, then the reduction --------------
   // Indices of packs beyond the chunk are clamped to the chunk's first pack so that all

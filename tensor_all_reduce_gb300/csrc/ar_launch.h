@@ -3,7 +3,16 @@
 
 #include <cuda_runtime.h>
 
+#include "ar.h"
+
 namespace ar {
+
+struct FusedParams;
+
+// Kernel parameters of one validated fused call, each CTA handling `chunk` packs of a row
+// and `csize` CTAs sharing a row (chunk = the row's packs and csize = 1: one CTA per row).
+// Shared by every entry point that launches a fused kernel.
+void fill_fused_params(FusedParams& p, const ar_fused_args& a, int chunk, int csize);
 
 // Kernel entry for a plain reduce: dtype (kF32/kF16/kBF16), n in 1..8, unroll 1 or 4,
 // vec = 16-byte path (else element-wise), has_tail = leftover packs/elements exist.

@@ -52,17 +52,24 @@ ar_status setup_current_device(int dev, DeviceSetup* out) {
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
       return AR_ERR_CUDA;
+    }
     if (major != 10 || minor != 3) return AR_ERR_UNSUPPORTED;
     const int max_dyn = optin - 1024;
     const void* fns[256];
     const int nf = ar::staged_kernel_list(fns, 256);
     for (int i = 0; i < nf; ++i)
-      if (cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn) != cudaSuccess)
+      if (cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, max_dyn) != cudaSuccess) {
+        (void)cudaGetLastError();
         return AR_ERR_CUDA;
+      }
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) return AR_ERR_CUDA;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      (void)cudaGetLastError();
+      return AR_ERR_CUDA;
+    }
     s.sm_count = sms;
     s.max_dyn_smem = max_dyn;
     s.scratch = static_cast<int*>(ptr);
@@ -94,7 +101,10 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_noalloc(const ar_fused_args* a, voi
   if (kStatusBytes > (size_t)AR_NOALLOC_SCRATCH_BYTES) return AR_ERR_UNSUPPORTED;
 
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return AR_ERR_CUDA;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
   if (dev < 0 || dev >= kMaxDevices) return AR_ERR_UNSUPPORTED;
   DeviceSetup ds;
   const ar_status st = setup_current_device(dev, &ds);
@@ -113,28 +123,8 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_noalloc(const ar_fused_args* a, voi
   if (block < 32) block = 32;
 
   ar::FusedParams p;
-  memset(&p, 0, sizeof(p));
-  for (int r = 0; r < a->n; ++r) p.x[r] = a->partials[r];
-  p.res_in = a->residual_in;
-  p.res_out = a->residual_out;
-  p.w = a->weight;
-  p.out = a->out;
-  p.q = static_cast<uint8_t*>(a->q_out);
-  p.scale = a->scale_out;
-  p.m = a->m;
-  p.h = (int)a->h;
-  p.row_packs = row_packs;
-  p.chunk_packs = row_packs;
-  p.csize = 1;
-  p.eps = a->eps;
-  p.inv_h = (float)(1.0 / (double)a->h);
-  p.gemma = a->gemma != 0;
-  p.skip_norm = a->skip_norm != 0;
-  p.out_f32 = a->out_fp32 != 0 && a->out != nullptr;
-  p.group_lanes = a->quant == AR_QUANT_FP8_E4M3_PER_GROUP ? a->group_size / 8 : 0;
-  p.ngroups = a->quant == AR_QUANT_FP8_E4M3_PER_GROUP ? (int)(a->h / a->group_size) : 0;
-  p.ld_in = a->ld_in;
-  p.ld_out = a->ld_out;
+  ar::fill_fused_params(p, *a, row_packs, 1);
+  p.prefetch = 1;
   ar::StagedParams sp = {};
   sp.stages = S;
   sp.row_bytes = (int)(a->h * es);
@@ -146,21 +136,29 @@ extern "C" ar_status ar_fused_reduce_rmsnorm_noalloc(const ar_fused_args* a, voi
   if (!fn) return AR_ERR_UNSUPPORTED;
   int per_sm = 1;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, block, (size_t)(S * stage_bytes)) != cudaSuccess ||
-      per_sm < 1)
+      per_sm < 1) {
+    (void)cudaGetLastError();  // the query's error is not the caller's
     per_sm = 1;
+  }
   const int64_t slots = (int64_t)ds.sm_count * per_sm;
   const int64_t grid = a->m < slots ? a->m : slots;
 
   // The status word must start at zero for this call; the previous call's value stays in
   // the array until this clear runs on `stream`.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (cudaMemsetAsync(ds.scratch, 0, kStatusBytes, s) != cudaSuccess) return AR_ERR_CUDA;
+  if (cudaMemsetAsync(ds.scratch, 0, kStatusBytes, s) != cudaSuccess) {
+    (void)cudaGetLastError();  // reported by the status; not left for the caller's next check
+    return AR_ERR_CUDA;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)grid, 1, 1);
   cfg.blockDim = dim3((unsigned)block, 1, 1);
   cfg.dynamicSmemBytes = (size_t)(S * stage_bytes);
   cfg.stream = s;
   void* args[2] = {&p, &sp};
-  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) return AR_ERR_CUDA;
+  if (cudaLaunchKernelExC(&cfg, fn, args) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
   return AR_OK;
 }

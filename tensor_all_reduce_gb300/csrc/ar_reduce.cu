@@ -78,9 +78,14 @@ __device__ __forceinline__ void reduce_one_elem(const ReduceParams& p, int64_t e
 
 template <int DT, int N, int UNROLL, bool HAS_TAIL>
 __global__ void __launch_bounds__(256) reduce_vec_kernel(const ReduceParams p) {
-  pdl_wait_and_release();
   const int64_t bs = blockDim.x;
   const int64_t tile = bs * UNROLL;
+  // this block's first tile into L2 while the previous grid may still run (see prefetch_l2)
+  if (p.prefetch && threadIdx.x == 0 && (int64_t)blockIdx.x < p.full_tiles) {
+#pragma unroll
+    for (int r = 0; r < N; ++r) prefetch_l2(static_cast<const uint4*>(p.x[r]) + blockIdx.x * tile, (uint32_t)(tile * 16));
+  }
+  pdl_wait_and_release();
   uint4* out = static_cast<uint4*>(p.out);
   for (int64_t t = blockIdx.x; t < p.full_tiles; t += gridDim.x) {
     const int64_t base = t * tile + threadIdx.x;

@@ -183,6 +183,17 @@ __device__ __forceinline__ void staged_rows(const FusedParams& p, const StagedPa
         for (int b = 0; b < 2; ++b) mbar_init(&rx_bar[k][b], 1);
     mbar_fence_init();
   }
+  // the first rows' inputs into L2 while the previous grid may still run (see prefetch_l2)
+  if (p.prefetch && threadIdx.x == 0) {
+    const int64_t pre = my_rows < S ? my_rows : S;
+    for (int64_t i = 0; i < pre; ++i) {
+      const size_t off = (size_t)(first + i * stride) * (size_t)(p.ld_in ? p.ld_in : (int64_t)p.h) * 2 +
+                         (size_t)col0 * 16;
+#pragma unroll
+      for (int r = 0; r < N; ++r) prefetch_l2((const uint8_t*)p.x[r] + off, row_bytes);
+      if (has_res) prefetch_l2((const uint8_t*)p.res_in + off, row_bytes);
+    }
+  }
   __syncthreads();
   if constexpr (CL) {  // every peer's receive barriers exist before anything is sent to them
     cluster_arrive();

@@ -41,6 +41,25 @@ def fused_inputs(n: int, m: int, h: int, dtype: str = "bf16", seed: int = 1234,
     return {"partials": partials, "residual": res, "weight": weight}
 
 
+def fill_fused_inputs_device(partials: List[torch.Tensor], residual: Optional[torch.Tensor], weight: torch.Tensor,
+                             seed: int, gemma: bool = False) -> None:
+    """The fused_inputs recipe drawn on the tensors' device (a generator of that device,
+    seeded) into existing [m, h] partials, residual and [h] weight: for tests that need fresh
+    inputs many times over without a host round trip."""
+    gen = torch.Generator(device=weight.device).manual_seed(seed)
+    for t in list(partials) + ([residual] if residual is not None else []):
+        t.copy_(torch.randn(t.shape, generator=gen, dtype=torch.float32, device=t.device))
+    wn = torch.randn(weight.shape, generator=gen, dtype=torch.float32, device=weight.device)
+    weight.copy_(0.1 * wn if gemma else 1.0 + 0.1 * wn)
+
+
+def fill_reduce_inputs_device(partials: List[torch.Tensor], seed: int) -> None:
+    """N(0, 1) values drawn on the tensors' device into existing flat partials."""
+    gen = torch.Generator(device=partials[0].device).manual_seed(seed)
+    for t in partials:
+        t.copy_(torch.randn(t.shape, generator=gen, dtype=torch.float32, device=t.device))
+
+
 def reduce_inputs(n: int, numel: int, dtype: str, seed: int = 1234) -> List[torch.Tensor]:
     """N flat ~N(0, 1) partials on the CPU."""
     gen = torch.Generator().manual_seed(seed)
@@ -168,8 +187,16 @@ def wide_rows() -> List[FusedWorkload]:
                           seed=1243)]
 
 
+def row_kernel_shape() -> List[FusedWorkload]:
+    """512 x 8192 (a shape of the fused-kernel test list on page "[HIP] fix(custom-ar): gfx1250
+    fused all-reduce + RMSNorm", Changes): 3-4 rows per SM on GB300, where every row's loads are
+    issued at once by one CTA per row."""
+    return [FusedWorkload("n4_m512_h8192_bf16_gemma_fp8", 4, 512, 8192, gemma=True, quant=True, mirror=True,
+                          seed=1244)]
+
+
 def all_fused() -> List[FusedWorkload]:
-    return small_fused() + decode_sweep() + gemma_fp8() + large_m() + wide_rows()
+    return small_fused() + decode_sweep() + gemma_fp8() + large_m() + wide_rows() + row_kernel_shape()
 
 
 def by_name(name: str):

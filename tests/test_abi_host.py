@@ -51,6 +51,7 @@ def test_null_context_queries(lib):
     assert lib.ar_get_info(None, tar.AR_INFO_SM_COUNT, ctypes.byref(v)) == tar.AR_ERR_NOT_INITIALIZED
     assert lib.ar_set_option(None, tar.AR_OPT_CLUSTER_SIZE, 4) == tar.AR_ERR_NOT_INITIALIZED
     assert lib.ar_set_option(None, tar.AR_OPT_TEST_STALL, 1) == tar.AR_ERR_NOT_INITIALIZED
+    assert lib.ar_set_option(None, tar.AR_OPT_L2_PREFETCH, 0) == tar.AR_ERR_NOT_INITIALIZED
     assert lib.ar_destroy(None) == tar.AR_OK
     assert tar.ar_last_variant(None) == ""
     assert lib.ar_init(None, 0, 0) == tar.AR_ERR_INVALID_ARG

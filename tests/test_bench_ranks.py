@@ -74,18 +74,47 @@ def test_reference_arm_under_two_ranks_only_rank0_prints():
     line = lines[0]
     assert line["impl"] == "reference" and line["unit"] == "us/call" and line["higher_is_better"] is False
     assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    sys.path.insert(0, ROOT)
+    import bench
+    from tensor_all_reduce_gb300 import synth
+    assert line["config"] == bench.workload_config(synth.by_name("n4_m16_h6144_bf16_plain"), 2)
+    assert line["rows_per_step"] == 16 and "whole call" in line["cpu_baseline"]["sample"]
+    # ms_per_step is the time a step took: steps x ms_per_step fits in the process's run time
+    assert line["ms_per_step"] * line["steps"] < 300_000
 
 
 def test_cpu_baseline_reports_serial_and_all_cores():
     sys.path.insert(0, ROOT)
     import bench
+    import oracle
     from tensor_all_reduce_gb300 import synth
     wl = synth.by_name("n4_m16_h6144_bf16_plain")
-    us, cores, rows = bench.oracle_all_cores_us(wl, seconds=0.3, runs=2)
-    assert us > 0 and cores == bench.host_cores() and 1 <= rows <= wl.m
-    cpu = bench.cpu_baseline(wl, seconds=0.3)
+    us, cores = bench.oracle_all_cores_us(bench.OracleInputs(wl), oracle.get(), runs=2)
+    assert us > 0 and cores == bench.host_cores()
+    cpu = bench.cpu_baseline(wl, budget_s=5.0)
     assert cpu["kind"] == "oracle" and cpu["cores"] == 1 and cpu["value"] > 0
+    assert "whole calls" in cpu["sample"]
     assert cpu["all_cores"]["cores"] == cores and cpu["all_cores"]["unit"] == cpu["unit"]
+
+
+def test_host_timings_take_whole_calls_when_they_fit():
+    sys.path.insert(0, ROOT)
+    import bench
+    from tensor_all_reduce_gb300 import synth
+    wl = synth.by_name("n8_m4096_h6144_bf16_plain")
+    assert bench.rows_for_budget(wl, 3.5, 25, 150.0) == wl.m           # 87.5 s of whole calls
+    rows = bench.rows_for_budget(wl, 10.0, 25, 150.0)                  # 250 s: a row sample
+    assert 1 <= rows < wl.m and rows * 10.0 / wl.m * 25 <= 150.0
+
+
+def test_headline_is_the_largest_configuration():
+    sys.path.insert(0, ROOT)
+    import bench
+    from tensor_all_reduce_gb300 import synth
+    wl = synth.by_name(bench.HEADLINE)
+    sizes = [w.algorithmic_bytes() for _, w in bench.config_workloads()]
+    assert wl.algorithmic_bytes() == max(sizes) and len(sizes) == 15
+    assert [t for t, _ in bench.config_workloads()] == ["C1"] + ["C2"] * 6 + ["C3"] * 4 + ["C4"] * 3 + ["C5"]
 
 
 def _leaving_worker(rank, world, port, q):

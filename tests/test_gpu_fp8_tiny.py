@@ -66,9 +66,10 @@ def tiny_rows_inputs(m, h, seed):
     mags = torch.pow(2.0, ks)
     inp["partials"] = [_scaled(p, mags) for p in inp["partials"]]
     inp["residual"] = _scaled(inp["residual"], mags)
-    for p in inp["partials"]:
-        p[3].zero_()
-    inp["residual"][3].zero_()
+    if m > 3:
+        for p in inp["partials"]:
+            p[3].zero_()
+        inp["residual"][3].zero_()
     return inp
 
 
@@ -154,6 +155,8 @@ FORMS = {
     "staged": ({tar.AR_OPT_FORCE_VARIANT: tar.VARIANT_STAGED}, "fused_staged"),
     "scalar": ({tar.AR_OPT_FORCE_VARIANT: tar.VARIANT_SCALAR}, "fused_scalar"),
 }
+# the element-wise form splits rows over a cluster when there are fewer rows than SMs
+ALSO = {"fused_scalar": "fused_cluster_scalar"}
 
 
 @pytest.mark.parametrize("case_name", list(CASES))
@@ -173,7 +176,7 @@ def test_tiny_fp8_every_kernel_form(ctx, dev, orc, case_name, form):
                              residual_out=ro, q_out=q, scale_out=sc, skip_norm=case["skip_norm"],
                              group_size=case["group"])
     torch.cuda.synchronize()
-    assert ctx.last_variant == variant, ctx.last_variant
+    assert ctx.last_variant in (variant, ALSO.get(variant)), ctx.last_variant
     _check(orc, case, _oracle(orc, inp, case), *_host(outs))
     _set(ctx, {})
 

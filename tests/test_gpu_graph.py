@@ -132,3 +132,100 @@ def test_graph_interleaved_calls(dev, orc):
             torch.cuda.synchronize()
             for c in calls:
                 c.check(orc)
+
+
+# ---------------------------------------------------------------------------
+# interleave stress: the mixed graph replayed 300 times with fresh inputs
+# ---------------------------------------------------------------------------
+
+class StressFused(FusedCall):
+    """Inputs drawn on the device every replay; checked in full (check_rows None) or on
+    `check_rows` sampled rows, plus a device-side scan that no NaN poison survived."""
+
+    def __init__(self, dev, n, m, h, dtype, gemma, quant, check_rows=None):
+        super().__init__(dev, n, m, h, dtype, gemma, quant)
+        self.check_rows = check_rows
+
+    def load(self, seed):
+        synth.fill_fused_inputs_device(self.parts, self.res, self.w, seed, self.gemma)
+
+    def check(self, orc, rng):
+        assert not bool(torch.isnan(self.out).any()) and not bool(torch.isnan(self.ro).any()), "poison left"
+        if self.quant:
+            assert not bool((self.q == 0x7F).any()) and not bool(torch.isnan(self.sc).any()), "poison left"
+        rows = (np.arange(self.m) if self.check_rows is None
+                else np.sort(rng.choice(self.m, self.check_rows, replace=False)))
+        idx = torch.from_numpy(rows).to(self.out.device)
+        take = lambda t: synth.bits(t.index_select(0, idx).cpu())
+        ref = orc.fused([take(p) for p in self.parts], take(self.res), synth.bits(self.w.cpu()), 1e-6, self.gemma,
+                        self.quant, self.dtype)
+        assert_bits_equal(take(self.ro), ref["res_out"], "graph residual_out")
+        y = take(self.out)
+        assert_y_within_ulp(y, ref["y"], self.dtype)
+        if self.quant:
+            assert_fp8(orc, self.q.index_select(0, idx).cpu().numpy(), self.sc.index_select(0, idx).cpu().numpy(),
+                       y, self.dtype, ref)
+
+
+class StressReduce(ReduceCall):
+    """Plain reduce with device-drawn inputs; checked in full or on `check_runs` sampled
+    contiguous runs of 4096 elements."""
+
+    def __init__(self, dev, n, numel, dtype, check_runs=None):
+        super().__init__(dev, n, numel, dtype)
+        self.check_runs = check_runs
+
+    def load(self, seed):
+        synth.fill_reduce_inputs_device(self.parts, seed)
+
+    def check(self, orc, rng):
+        assert not bool(torch.isnan(self.out).any()), "poison left"
+        if self.check_runs is None:
+            sl = [slice(0, self.numel)]
+        else:
+            starts = rng.choice(self.numel // 4096, self.check_runs, replace=False) * 4096
+            sl = [slice(int(a), int(a) + 4096) for a in starts]
+        for s in sl:
+            ref = orc.reduce_sum([synth.bits(p[s].cpu()) for p in self.parts], self.dtype)
+            assert_bits_equal(synth.bits(self.out[s].cpu()), ref, "graph reduce")
+
+
+def test_graph_interleaved_300_replays(dev, orc):
+    """The mixed graph of decode-sized, large, FP8, element-wise, cluster and plain-reduce calls
+    replayed 300 times; before every replay each call gets fresh inputs and NaN-poisoned
+    outputs.  Small calls are checked in full on every replay, large ones on sampled rows."""
+    calls = [
+        StressFused(dev, 4, 16, 6144, "bf16", False, False),
+        StressReduce(dev, 4, 1025 * 512, "fp16"),
+        StressFused(dev, 4, 384, 6144, "bf16", True, True, check_rows=3),
+        StressFused(dev, 4, 1, 6144, "bf16", False, False),
+        StressReduce(dev, 4, 1024 * 512, "fp32"),
+        StressFused(dev, 8, 1024, 6144, "bf16", False, False, check_rows=2),
+        StressFused(dev, 4, 7, 6145, "fp16", True, True),
+        StressFused(dev, 4, 64, 12288, "bf16", True, True, check_rows=2),
+        StressReduce(dev, 5, 8192 * 16 * 152, "bf16", check_runs=2),
+        StressFused(dev, 2, 3, 2880, "fp16", False, True),      # short fp16 rows with FP8
+    ]
+    rng = np.random.default_rng(2024)
+    with tar.Context(0) as ctx:
+        for i, c in enumerate(calls):
+            c.load(seed=i)
+            c.call(ctx)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.graph(g, stream=s):
+            for c in calls:
+                c.call(ctx)
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        for rep in range(300):
+            for i, c in enumerate(calls):
+                c.load(seed=7919 * (rep + 1) + i)
+                c.poison()
+            g.replay()
+            torch.cuda.synchronize()
+            for c in calls:
+                c.check(orc, rng)
+        assert ctx.device_status() == 0

@@ -463,3 +463,32 @@ def test_tall_call_sampled_rows(ctx, dev, orc):
     ref = oracle_fused(orc, sub, "bf16", gemma=True, quant=True)
     pick = {k: (v[rows] if v is not None and k != "variant" else v) for k, v in got.items()}
     check_fused(orc, pick, ref, "bf16", True)
+
+
+# ---------------------------------------------------------------------------
+# L2 prefetch ahead of the grid-dependency wait
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("variant", [tar.VARIANT_AUTO, tar.VARIANT_ROW, tar.VARIANT_STAGED, tar.VARIANT_CLUSTER])
+def test_prefetch_changes_no_bit(ctx, dev, variant):
+    """The kernels' L2 prefetch of their first inputs (issued before they wait for the previous
+    kernel) is a hint only: every output is bit-identical with it on and off, including when
+    the previous kernel on the stream writes the inputs of the next call."""
+    ctx.set_option(tar.AR_OPT_FORCE_VARIANT, variant)
+    inp = synth.fused_inputs(4, 300, 6144, "bf16", seed=41, gemma=True)
+    parts = to_dev(inp["partials"], dev)
+    res, w = inp["residual"].to(dev), inp["weight"].to(dev)
+    outs = {}
+    for pf in (0, 1):
+        ctx.set_option(tar.AR_OPT_L2_PREFETCH, pf)
+        # the first call writes into a partial of the second (a producer right before its consumer)
+        p2 = [p.clone() for p in parts]
+        ctx.fused_reduce_rmsnorm(parts, res, w, eps=1e-6, gemma=True, quant=False, out=p2[1], want_residual_out=False)
+        y, ro, q, sc = ctx.fused_reduce_rmsnorm(p2, res, w, eps=1e-6, gemma=True, quant=True)
+        rs = torch.empty_like(parts[0])
+        ctx.reduce_sum(p2, out=rs)
+        torch.cuda.synchronize()
+        outs[pf] = [bits_of(y), bits_of(ro), q.cpu().numpy(), sc.cpu().numpy(), bits_of(rs)]
+    ctx.set_option(tar.AR_OPT_L2_PREFETCH, 1)
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)
