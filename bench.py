@@ -613,7 +613,7 @@ def sweep(ctx, dev, l2, peak):
     import torch
     from tensor_all_reduce_gb300 import synth
     out = [time_workload(ctx, dev, wl, l2, peak)
-           for wl in synth.wide_rows() + synth.row_kernel_shape() + synth.options() + synth.reduce_large()]
+           for wl in synth.wide_rows() + synth.mid_batch() + synth.options() + synth.reduce_large()]
     # 8 independent decode calls (16 x 6144 each): one batched launch against 8 launches
     wl = synth.FusedWorkload("n4_m16_h6144_bf16_decode", 4, 16, 6144, seed=1236)
     k = 8
@@ -692,7 +692,11 @@ def run_case(args, dev):
     import tensor_all_reduce_gb300 as tar
     from tensor_all_reduce_gb300 import synth
     wl = synth.by_name(args.case)
+    if args.case_rows and isinstance(wl, synth.FusedWorkload):   # the same call on fewer rows
+        import dataclasses
+        wl = dataclasses.replace(wl, m=args.case_rows, name=f"{wl.name} ({args.case_rows} rows)")
     with tar.Context(dev.index or 0) as ctx:
+        ctx.set_option(tar.AR_OPT_FORCE_VARIANT, args.force_variant)
         l2 = ctx.info(tar.AR_INFO_L2_BYTES)
         fused = isinstance(wl, synth.FusedWorkload)
         R = rotation_sets(wl.algorithmic_bytes(), l2, cap=64)
@@ -726,6 +730,9 @@ def main(argv=None):
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--case", default=None, help="run only `--case-calls` eager calls of this workload")
     p.add_argument("--case-calls", type=int, default=3)
+    p.add_argument("--case-rows", type=int, default=0, help="with --case: run the fused workload on this many rows")
+    p.add_argument("--force-variant", type=int, default=0,
+                   help="with --case: AR_OPT_FORCE_VARIANT (0 auto, 1 row, 2 cluster, 3 staged, 4 element-wise)")
     args = p.parse_args(argv)
     world, rank, local = dist_env()
     if args.impl == "reference":

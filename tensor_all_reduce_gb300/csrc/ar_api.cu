@@ -452,7 +452,10 @@ ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int
     const int64_t tile = (int64_t)kReduceBlock * unroll;
     p.full_tiles = p.npacks / tile;
     const bool has_tail = (p.npacks % tile) != 0 || (numel % epp) != 0;
-    int64_t gr = p.full_tiles < max_grid ? p.full_tiles : max_grid;
+    // with room in the grid the tail gets a block of its own (block full_tiles owns it), so
+    // it runs beside the full tiles instead of after one of them
+    const int64_t want = p.full_tiles + (has_tail ? 1 : 0);
+    int64_t gr = want < max_grid ? want : max_grid;
     if (gr < 1) gr = 1;
     grid = (unsigned)gr;
     fn = ar::reduce_kernel(dtype, n, unroll, true, has_tail);
@@ -666,13 +669,13 @@ static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, b
   int S = ctx->stages ? ctx->stages : (one_row_per_cta ? 1 : 2);
   if (!ctx->stages && S * stage_bytes > ctx->max_dyn_smem) S = 1;
   const bool staged_ok = vec && row_packs <= 1024 && S * stage_bytes <= ctx->max_dyn_smem;
-  // Automatic choice (same-GPU sweeps on GB300, N = 4, h = 6144, m = 1 .. 512, with and
-  // without FP8): up to two rows per SM -> one staged CTA per row, all resident at once
-  // (bulk row loads have the lowest latency: 4.4 against 5.8 us for the row kernel at
-  // m = 152); 2..3 rows per SM -> the persistent staged kernel; 3..4 rows per SM -> the row
-  // kernel (every row's loads in flight at once); more -> the persistent staged kernel.
-  const bool staged_auto = ctx->force_variant == 0 && ctx->cluster_size == 0 && ctx->ppt == 0 &&
-                           (a->m < 3LL * ctx->sm_count || a->m >= 4LL * ctx->sm_count);
+  // Automatic choice: the staged kernel for every batch of 16-byte-aligned rows of at most
+  // 8192 elements; up to two rows per SM with one CTA per row, all resident at once, else
+  // persistent.  Same-GPU sweeps on GB300 (N = 4, h = 6144 and 8192, m = 1 .. 4096, with
+  // the L2 prefetch ahead of the grid-dependency wait): the per-thread-load row kernel was
+  // slower at every size, also at three to four rows per SM where it once led (m = 600:
+  // 10.1 against 11.2 us; 512 x 8192: 11.1 against 14.1 us).
+  const bool staged_auto = ctx->force_variant == 0 && ctx->cluster_size == 0 && ctx->ppt == 0;
   if (host && ctx->force_variant == 3) return AR_ERR_UNSUPPORTED;
   if (!host && (ctx->force_variant == 3 || (staged_auto && staged_ok))) {
     if (!staged_ok) return AR_ERR_UNSUPPORTED;

@@ -80,10 +80,21 @@ template <int DT, int N, int UNROLL, bool HAS_TAIL>
 __global__ void __launch_bounds__(256) reduce_vec_kernel(const ReduceParams p) {
   const int64_t bs = blockDim.x;
   const int64_t tile = bs * UNROLL;
-  // this block's first tile into L2 while the previous grid may still run (see prefetch_l2)
-  if (p.prefetch && threadIdx.x == 0 && (int64_t)blockIdx.x < p.full_tiles) {
+  // this block's first tile (or the tail packs it owns) into L2 while the previous grid may
+  // still run (see prefetch_l2)
+  if (p.prefetch && threadIdx.x == 0) {
+    int64_t first = -1, packs = 0;
+    if ((int64_t)blockIdx.x < p.full_tiles) {
+      first = (int64_t)blockIdx.x * tile;
+      packs = tile;
+    } else if (HAS_TAIL && blockIdx.x == (unsigned)(p.full_tiles % gridDim.x)) {
+      first = p.full_tiles * tile;
+      packs = p.npacks - first;
+    }
+    if (packs > 0) {
 #pragma unroll
-    for (int r = 0; r < N; ++r) prefetch_l2(static_cast<const uint4*>(p.x[r]) + blockIdx.x * tile, (uint32_t)(tile * 16));
+      for (int r = 0; r < N; ++r) prefetch_l2(static_cast<const uint4*>(p.x[r]) + first, (uint32_t)(packs * 16));
+    }
   }
   pdl_wait_and_release();
   uint4* out = static_cast<uint4*>(p.out);

@@ -187,16 +187,16 @@ def wide_rows() -> List[FusedWorkload]:
                           seed=1243)]
 
 
-def row_kernel_shape() -> List[FusedWorkload]:
+def mid_batch() -> List[FusedWorkload]:
     """512 x 8192 (a shape of the fused-kernel test list on page "[HIP] fix(custom-ar): gfx1250
-    fused all-reduce + RMSNorm", Changes): 3-4 rows per SM on GB300, where every row's loads are
-    issued at once by one CTA per row."""
+    fused all-reduce + RMSNorm", Changes): 3-4 rows per SM on GB300, between the decode
+    sizes and the long streaming batches."""
     return [FusedWorkload("n4_m512_h8192_bf16_gemma_fp8", 4, 512, 8192, gemma=True, quant=True, mirror=True,
                           seed=1244)]
 
 
 def all_fused() -> List[FusedWorkload]:
-    return small_fused() + decode_sweep() + gemma_fp8() + large_m() + wide_rows() + row_kernel_shape()
+    return small_fused() + decode_sweep() + gemma_fp8() + large_m() + wide_rows() + mid_batch()
 
 
 def by_name(name: str):
