@@ -297,9 +297,9 @@ typedef enum {
   AR_INFO_L2_BYTES = 1,
   AR_INFO_REDUCE_TILE_PACKS = 2, /* 16-byte packs per tile of the per-thread reduce kernel:
                                     with AR_OPT_REDUCE_UNROLL forced, of that form; else of the
-                                    four-pack form (the automatic choice also uses one-pack
-                                    tiles of 256 packs, a divisor, for small arrays and 16-bit
-                                    sums of six or more partials) */
+                                    four-pack form (the automatic choice uses it for 16-bit sums
+                                    of one to three partials of at least one wave of tiles, and
+                                    one-pack tiles of 256 packs, a divisor, otherwise) */
   AR_INFO_DEVICE = 3
 } ar_info;
 ar_status ar_get_info(const ar_ctx* ctx, ar_info key, int64_t* value);

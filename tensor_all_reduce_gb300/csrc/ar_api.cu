@@ -442,13 +442,15 @@ ar_status ar_reduce_sum(ar_ctx* ctx, void* out, const void* const* partials, int
   if (vec) {
     const int epp = 16 / es;
     p.npacks = numel / epp;
-    // Four packs per thread per tile for large arrays, except with 16-bit elements and six
-    // or more partials, where one pack streams far better (same-GPU sweep on GB300, 6M and
-    // 25M elements: bf16 N = 8 at 104 % of the measured copy bandwidth with one pack against
-    // 73 % with four, N = 6 97 % against 82 %; N <= 4 and fp32 gain 1-9 % from four).
+    // Four packs per thread per tile only for 16-bit sums of one to three partials that fill
+    // at least one wave of single-pack tiles; one pack otherwise.  Same-GPU A/B on GB300 with
+    // the L2 prefetch (us/call, HBM-cold, four packs against one): bf16 N = 2, 6.3M elements
+    // 6.39 / 7.17, 25M 24.21 / 23.88; N = 3, 25M 34.01 / 34.21; N = 8, 25M 90.89 / 68.33;
+    // fp16 N = 4, 3.1M 8.30 / 6.16; fp32 N = 2 / 4 / 8, 25M 47.24 / 46.66, 78.91 / 77.41,
+    // 140.08 / 138.20; fp32 N = 4, 6.3M 23.77 / 20.94.
     int unroll = ctx->reduce_unroll;
     if (unroll == 0)
-      unroll = (p.npacks >= (int64_t)max_grid * kReduceBlock * 4 && (es == 4 || n <= 4)) ? 4 : 1;
+      unroll = (es == 2 && n <= 3 && p.npacks >= (int64_t)max_grid * kReduceBlock) ? 4 : 1;
     const int64_t tile = (int64_t)kReduceBlock * unroll;
     p.full_tiles = p.npacks / tile;
     const bool has_tail = (p.npacks % tile) != 0 || (numel % epp) != 0;
