@@ -686,7 +686,24 @@ static ar_status fused_impl(ar_ctx* ctx, const ar_fused_args* a, void* stream, b
     // on N = 4, 2800 x 6144 with per-token and per-group FP8, without FP8 and with fp32
     // output; 2 packs on 1024 rows, on N = 8 and without the norm)
     const bool one_pack = a->n <= 4 && !a->skip_norm && a->m >= 8LL * ctx->sm_count && row_packs <= 1024;
-    const int sppt = ctx->ppt ? ctx->ppt : (one_pack ? 1 : 2);
+    int sppt = ctx->ppt ? ctx->ppt : (one_pack ? 1 : 2);
+    // One CTA per row with some SMs holding two rows, without FP8: one pack per thread when two
+    // such CTAs still fit on an SM (same-GPU A/B on GB300, us/call HBM-cold, one pack against
+    // two: N = 4, h = 6144, m = 200 / 256 / 300: 4.13 / 4.70, 4.59 / 4.77, 5.15 / 5.34;
+    // h = 4096, m = 256: 3.78 / 4.43; with FP8 one pack was 2-6 % slower, at m = 152 2 %
+    // slower, and at N = 8 its 54 registers a thread leave room for one CTA per SM: 28 % slower).
+    if (!ctx->ppt && !one_pack && !quant && !a->skip_norm && a->m > ctx->sm_count && a->m <= 2LL * ctx->sm_count) {
+      const void* f1 = a->dtype == AR_DTYPE_BF16 ? ar::staged_kernel_bf16(a->n, 1, false)
+                                                 : ar::staged_kernel_f16(a->n, 1, false);
+      const int b1 = (row_packs + 31) / 32 * 32;
+      DeviceGuard og(ctx->device);
+      int fit = 0;
+      if (f1 && cudaOccupancyMaxActiveBlocksPerMultiprocessor(&fit, f1, b1, (size_t)(S * stage_bytes)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        fit = 0;
+      }
+      if (fit >= 2) sppt = 1;
+    }
     int sblock = ((row_packs + sppt - 1) / sppt + 31) / 32 * 32;
     if (sblock < 32) sblock = 32;
     ar::FusedParams p;

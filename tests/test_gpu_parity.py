@@ -186,6 +186,19 @@ def test_fused_every_variant(ctx, dev, orc, name, opts, m, h):
             assert got["variant"] == "fused_row_vec"
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("m", [151, 152, 153, 256, 304, 305])
+def test_fused_one_to_two_rows_per_sm(ctx, dev, orc, m, dtype):
+    """Around the one-CTA-per-row regime (one to two rows per SM), where the automatic choice
+    switches stage count and, for rows without FP8, packs per thread: every form it picks
+    against the oracle, with and without FP8, for 4 and 8 partials."""
+    for n, h, quant in ((4, 6144, False), (4, 4096, False), (8, 6144, False), (4, 6144, True)):
+        inp = synth.fused_inputs(n, m, h, dtype, seed=m * 3 + h + n, gemma=quant)
+        got = run_fused(ctx, dev, inp, dtype, gemma=quant, quant=quant)
+        assert got["variant"] == "fused_staged", got["variant"]
+        check_fused(orc, got, oracle_fused(orc, inp, dtype, gemma=quant, quant=quant), dtype, quant)
+
+
 @pytest.mark.parametrize("n", range(1, 9))
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 def test_fused_every_n(ctx, dev, orc, n, dtype):
@@ -489,6 +502,30 @@ def test_prefetch_changes_no_bit(ctx, dev, variant):
         ctx.reduce_sum(p2, out=rs)
         torch.cuda.synchronize()
         outs[pf] = [bits_of(y), bits_of(ro), q.cpu().numpy(), sc.cpu().numpy(), bits_of(rs)]
+    ctx.set_option(tar.AR_OPT_L2_PREFETCH, 1)
+    for a, b in zip(outs[0], outs[1]):
+        assert np.array_equal(a, b)
+
+
+def test_prefetch_changes_no_bit_cluster_and_batch(ctx, dev):
+    """The same for the staged cluster form (rows split over CTAs, each prefetching its slice)
+    and the batched kernel (each CTA prefetching its call's row)."""
+    inp = synth.fused_inputs(4, 40, 16384, "bf16", seed=43, gemma=True)
+    parts = to_dev(inp["partials"], dev)
+    res, w = inp["residual"].to(dev), inp["weight"].to(dev)
+    small = [synth.fused_inputs(2, m, 4096, "bf16", seed=44 + m) for m in (3, 17, 1)]
+    outs = {}
+    for pf in (0, 1):
+        ctx.set_option(tar.AR_OPT_L2_PREFETCH, pf)
+        y, ro, q, sc = ctx.fused_reduce_rmsnorm(parts, res, w, eps=1e-6, gemma=True, quant=True)
+        assert ctx.last_variant == "fused_staged_cluster"
+        calls = [{"partials": to_dev(s["partials"], dev), "residual": s["residual"].to(dev),
+                  "weight": s["weight"].to(dev), "quant": True} for s in small]
+        res_b = ctx.fused_reduce_rmsnorm_batch(calls)
+        assert ctx.last_variant == "fused_batch"
+        torch.cuda.synchronize()
+        outs[pf] = [bits_of(y), bits_of(ro), q.cpu().numpy(), sc.cpu().numpy()] + \
+                   [x.view(torch.uint8).cpu().numpy() for r in res_b for x in r if x is not None]
     ctx.set_option(tar.AR_OPT_L2_PREFETCH, 1)
     for a, b in zip(outs[0], outs[1]):
         assert np.array_equal(a, b)
