@@ -55,6 +55,10 @@ MUTANTS = [
     ("group_bounds_off_by_one", "const int64_t j0 = k * g, j1 = j0 + g;", "const int64_t j0 = k * g, j1 = j0 + g - 1;"),
     ("group_scale_index", "scale + r * (h / group), (const uint16_t*)y + r * h", "scale + r, (const uint16_t*)y + r * h"),
     ("group_max_448_240", "    float sc = amax / 448.0f;\n    scale[k] = sc;", "    float sc = amax / 240.0f;\n    scale[k] = sc;"),
+    ("fp8_quotient_by_reciprocal", "float v = load_elem(y, base + j, dtype) / sc;",
+     "float v = load_elem(y, base + j, dtype) * (1.0f / sc);"),
+    ("fp8_scale_flushes_subnormals", "  float sc = amax / 448.0f;\n  scale[row] = sc;",
+     "  float sc = amax / 448.0f;\n  if (sc < 1.17549435e-38f) sc = 0.0f;\n  scale[row] = sc;"),
 ]
 
 
