@@ -699,8 +699,12 @@ def run_case(args, dev):
         ctx.set_option(tar.AR_OPT_FORCE_VARIANT, args.force_variant)
         l2 = ctx.info(tar.AR_INFO_L2_BYTES)
         fused = isinstance(wl, synth.FusedWorkload)
-        R = rotation_sets(wl.algorithmic_bytes(), l2, cap=64)
-        sets = (FusedSets if fused else ReduceSets)(wl, R, dev)
+        if args.case_batch and fused:       # `case_batch` independent calls of the workload, one launch
+            R = rotation_sets(args.case_batch * wl.algorithmic_bytes(), l2, cap=64)
+            sets = BatchSets(wl, args.case_batch, R, dev, batched=True)
+        else:
+            R = rotation_sets(wl.algorithmic_bytes(), l2, cap=64)
+            sets = (FusedSets if fused else ReduceSets)(wl, R, dev)
         for i in range(args.warmup):
             sets.call(ctx, i)
         torch.cuda.synchronize()
@@ -712,8 +716,8 @@ def run_case(args, dev):
         end.synchronize()
         us = start.elapsed_time(end) * 1000.0 / max(args.case_calls, 1)
         print(json.dumps({"case": wl.name, "variant": ctx.last_variant, "calls": args.case_calls, "warmup": args.warmup,
-                          "buffer_sets": R, "us_per_call_eager": round(us, 3),
-                          "bytes_per_call": wl.algorithmic_bytes()}), flush=True)
+                          "batch": args.case_batch, "buffer_sets": R, "us_per_call_eager": round(us, 3),
+                          "bytes_per_call": wl.algorithmic_bytes() * max(1, args.case_batch)}), flush=True)
     return 0
 
 
@@ -731,6 +735,8 @@ def main(argv=None):
     p.add_argument("--case", default=None, help="run only `--case-calls` eager calls of this workload")
     p.add_argument("--case-calls", type=int, default=3)
     p.add_argument("--case-rows", type=int, default=0, help="with --case: run the fused workload on this many rows")
+    p.add_argument("--case-batch", type=int, default=0,
+                   help="with --case: each call is this many independent calls of the workload in one batched launch")
     p.add_argument("--force-variant", type=int, default=0,
                    help="with --case: AR_OPT_FORCE_VARIANT (0 auto, 1 row, 2 cluster, 3 staged, 4 element-wise)")
     args = p.parse_args(argv)
