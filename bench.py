@@ -202,13 +202,15 @@ class FusedSets:
         t = synth.TORCH_DTYPES[wl.dtype]
         m, h, n = wl.m, wl.h, wl.n
         inp = wl.inputs()
-        self.parts = torch.empty((sets, n, m, h), dtype=t, device=dev)
-        self.res = torch.empty((sets, m, h), dtype=t, device=dev) if wl.residual else None
+        hp = h + wl.pad                     # padded rows: [m, h] views of [m, h + pad] buffers
+        self.parts = torch.empty((sets, n, m, hp), dtype=t, device=dev)[..., :h]
+        self.res = torch.empty((sets, m, hp), dtype=t, device=dev)[..., :h] if wl.residual else None
         self.w = inp["weight"].to(dev)
         want_y = wl.mirror or not wl.quant
-        self.out = torch.empty((sets, m, h), dtype=torch.float32 if wl.out_fp32 else t, device=dev) if want_y else None
-        self.ro = torch.empty((sets, m, h), dtype=t, device=dev) if wl.residual else None
-        self.q = torch.empty((sets, m, h), dtype=torch.uint8, device=dev) if wl.quant else None
+        self.out = (torch.empty((sets, m, hp), dtype=torch.float32 if wl.out_fp32 else t, device=dev)[..., :h]
+                    if want_y else None)
+        self.ro = torch.empty((sets, m, hp), dtype=t, device=dev)[..., :h] if wl.residual else None
+        self.q = torch.empty((sets, m, hp), dtype=torch.uint8, device=dev)[..., :h] if wl.quant else None
         ns = m * (h // wl.group) if wl.group else m
         self.sc = torch.empty((sets, ns), dtype=torch.float32, device=dev) if wl.quant else None
         for k in range(n):
@@ -613,7 +615,8 @@ def sweep(ctx, dev, l2, peak):
     import torch
     from tensor_all_reduce_gb300 import synth
     out = [time_workload(ctx, dev, wl, l2, peak)
-           for wl in synth.wide_rows() + synth.mid_batch() + synth.options() + synth.reduce_large()]
+           for wl in synth.wide_rows() + synth.mid_batch() + synth.options() + synth.padded_rows()
+           + synth.reduce_large()]
     # 8 independent decode calls (16 x 6144 each): one batched launch against 8 launches
     wl = synth.FusedWorkload("n4_m16_h6144_bf16_decode", 4, 16, 6144, seed=1236)
     k = 8

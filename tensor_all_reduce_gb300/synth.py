@@ -102,6 +102,7 @@ class FusedWorkload:
     skip_norm: bool = False      # all-reduce (+ residual) + per-token FP8 without RMSNorm
     out_fp32: bool = False       # the normed output stored as fp32
     group: int = 0               # per-group FP8 with this many elements per group (0: per token)
+    pad: int = 0                 # rows of inputs and outputs padded by this many elements (row stride h + pad)
 
     def inputs(self) -> Dict[str, object]:
         return fused_inputs(self.n, self.m, self.h, self.dtype, self.seed, self.gemma, self.residual)
@@ -179,6 +180,13 @@ def options() -> List[FusedWorkload]:
                           mirror=True, group=128, seed=1241)]
 
 
+def padded_rows() -> List[FusedWorkload]:
+    """The every-step call on padded rows (row stride 6144 + 64 for inputs and outputs): the
+    fused path on [m, h] views of wider buffers."""
+    return [FusedWorkload("n4_m2800_h6144_bf16_gemma_fp8_pad64", 4, 2800, 6144, gemma=True, quant=True, mirror=True,
+                          seed=1245, pad=64)]
+
+
 def wide_rows() -> List[FusedWorkload]:
     """Rows longer than 8192 elements (hidden sizes of larger models), split over a cluster."""
     return [FusedWorkload("n4_m2048_h12288_bf16_gemma_fp8", 4, 2048, 12288, gemma=True, quant=True, mirror=True,
@@ -200,7 +208,7 @@ def all_fused() -> List[FusedWorkload]:
 
 
 def by_name(name: str):
-    for w in all_fused() + options() + reduce_only() + reduce_large():
+    for w in all_fused() + options() + padded_rows() + reduce_only() + reduce_large():
         if w.name == name:
             return w
     raise KeyError(name)

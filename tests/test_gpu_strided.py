@@ -133,3 +133,30 @@ def test_padded_rows_batched(ctx, dev, orc):
                         synth.bits(inp["weight"]), 1e-6, False, False, "bf16")
         assert_bits_equal(bits_of(ro.contiguous()), ref["res_out"], "residual_out")
         assert_y_within_ulp(bits_of(y.contiguous()), ref["y"], "bf16")
+
+
+@pytest.mark.parametrize("wl", synth.padded_rows(), ids=[w.name for w in synth.padded_rows()])
+def test_padded_workload_full_size(ctx, dev, orc, wl):
+    """The benchmark's padded-row workload at its full size, in the launch configuration the
+    benchmark times (the automatic choice): the staged kernel on [m, h] views of [m, h + pad]
+    buffers, checked against the oracle on the contiguous copies."""
+    _set(ctx, {})
+    inp = wl.inputs()
+    m, h = wl.m, wl.h
+    parts = [_padded(p, wl.pad, dev)[1] for p in inp["partials"]]
+    res = _padded(inp["residual"], wl.pad, dev)[1]
+    y_big, y = _padded(inp["residual"], wl.pad, dev, fill=0xA5)
+    ro_big, ro = _padded(inp["residual"], wl.pad, dev, fill=0xA5)
+    q_big = torch.full((m, h + wl.pad), 0xA5, dtype=torch.uint8, device=dev)
+    sc = torch.empty((m,), dtype=torch.float32, device=dev)
+    ctx.fused_reduce_rmsnorm(parts, res, inp["weight"].to(dev), eps=1e-6, gemma=wl.gemma, quant=wl.quant, out=y,
+                             residual_out=ro, q_out=q_big[:, :h], scale_out=sc)
+    torch.cuda.synchronize()
+    assert ctx.last_variant == "fused_staged"
+    ref = orc.fused([synth.bits(p) for p in inp["partials"]], synth.bits(inp["residual"]), synth.bits(inp["weight"]),
+                    1e-6, wl.gemma, wl.quant, "bf16")
+    assert_bits_equal(bits_of(ro), ref["res_out"], "residual_out")
+    yb = bits_of(y)
+    assert_y_within_ulp(yb, ref["y"], "bf16")
+    assert_fp8(orc, q_big[:, :h].cpu().numpy(), sc.cpu().numpy(), yb, "bf16", ref)
+    assert _pads_intact(y_big, h, 0xA5) and _pads_intact(ro_big, h, 0xA5) and _pads_intact(q_big, h, 0xA5)
