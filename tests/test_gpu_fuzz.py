@@ -229,3 +229,110 @@ def test_random_batch(ctx, dev, orc, k):
             q_ref, s_ref = orc.per_token_quant(y16, dtype)
             assert np.array_equal(sc.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), what
             assert np.array_equal(q.cpu().numpy(), q_ref), what
+
+
+# ---------------------------------------------------------------------------
+# the other entry points: host buffers and the allocation-free call
+# ---------------------------------------------------------------------------
+
+def _check_fused(orc, c, inp, ro, y, q, sc, what):
+    """The bars of test_random_configuration for outputs already copied to the host."""
+    dt = c["dtype"]
+    ref = orc.fused_ex([synth.bits(p) for p in inp["partials"]], synth.bits(inp["residual"]),
+                       None if c["skip_norm"] else synth.bits(inp["weight"]), 1e-6, c["gemma"], c["quant"], dt,
+                       skip_norm=c["skip_norm"], out_fp32=c["out_fp32"], group=c["group"])
+    assert_bits_equal(synth.bits(ro), ref["res_out"], f"residual_out, {what}")
+    y16 = None
+    if y is not None and c["out_fp32"]:
+        g32, r32 = y.numpy().astype(np.float64), ref["y32"].astype(np.float64)
+        assert np.all(np.abs(g32 - r32) <= F32_REL_TOL * np.abs(r32) + 1e-30), what
+    elif y is not None:
+        y16 = synth.bits(y)
+        if c["skip_norm"]:
+            assert_bits_equal(y16, ref["y"], f"output (= z), {what}")
+        else:
+            assert_y_within_ulp(y16, ref["y"], dt, f"y, {what}")
+    if c["quant"]:
+        qg, sg = q.numpy(), sc.numpy()
+        if y16 is not None:
+            q_ref, s_ref = orc.per_group_quant(y16, c["group"], dt) if c["group"] else orc.per_token_quant(y16, dt)
+            assert np.array_equal(sg.view(np.uint32), s_ref.view(np.uint32)), f"scales, {what}"
+            assert np.array_equal(qg, q_ref), f"codes, {what}"
+        else:
+            tol = 2.0 ** -7 if dt == "bf16" else 2.0 ** -10
+            s_g, s_r = sg.astype(np.float64), ref["scale"].astype(np.float64)
+            assert np.all(np.abs(s_g - s_r) <= tol * s_r * 1.0001), f"scales, {what}"
+            assert np.abs(code_ordinal(qg) - code_ordinal(ref["q"])).max(initial=0) <= 1, f"codes, {what}"
+
+
+@pytest.mark.parametrize("k", range(40))
+def test_random_configuration_host_buffers(ctx, dev, orc, k):
+    """Random configurations through ar_fused_reduce_rmsnorm_host, every buffer page-locked
+    host memory (padded rows included)."""
+    c = draw(1000 + k)
+    n, m, h, dt = c["n"], c["m"], c["h"], c["dtype"]
+    if m == 0:
+        return
+    m = min(m, 64)                                     # host memory is read across the CPU-GPU link
+    inp = synth.fused_inputs(n, m, h, dt, seed=c["seed"], gemma=c["gemma"], residual=c["residual"])
+
+    def pinned(t, pad):
+        big = torch.empty((m, h + pad), dtype=t.dtype, pin_memory=True)
+        big[:, :h].copy_(t)
+        return big[:, :h]
+
+    parts = [pinned(p, c["pad_in"]) for p in inp["partials"]]
+    res = pinned(inp["residual"], c["pad_in"]) if c["residual"] else None
+    w = None if c["skip_norm"] else inp["weight"].pin_memory()
+    t16 = TDT[dt]
+    zeros = lambda dtype: torch.zeros((m, h), dtype=dtype)
+    ro = pinned(zeros(t16), c["pad_out"])
+    y = pinned(zeros(torch.float32 if c["out_fp32"] else t16), c["pad_out"]) if c["mirror"] else None
+    q = pinned(zeros(torch.uint8), c["pad_out"]) if c["quant"] else None
+    sc = (torch.empty((m, h // c["group"]) if c["group"] else (m,), dtype=torch.float32, pin_memory=True)
+          if c["quant"] else None)
+    ctx.fused_reduce_rmsnorm_host(parts, res, w, eps=1e-6, gemma=c["gemma"], quant=c["quant"], out=y, residual_out=ro,
+                                  q_out=q, scale_out=sc, want_out=c["mirror"], skip_norm=c["skip_norm"],
+                                  out_fp32=c["out_fp32"], group_size=c["group"])
+    torch.cuda.synchronize()
+    what = f"host case {k} {c} m={m} ({ctx.last_variant})"
+    if y is None and c["skip_norm"]:
+        y = ro
+    _check_fused(orc, c, inp, ro.clone(), None if y is None else y.clone(), None if q is None else q.clone(),
+                 None if sc is None else sc.clone(), what)
+
+
+@pytest.mark.parametrize("k", range(40))
+def test_random_configuration_noalloc(dev, orc, k):
+    """Random configurations (16-byte-aligned rows of at most 8192 elements, what the entry
+    takes) through the allocation-free ar_fused_reduce_rmsnorm_noalloc."""
+    c = draw(2000 + k)
+    n, m, dt = c["n"], c["m"], c["dtype"]
+    h = max(8, min(8192, c["h"] // 8 * 8))
+    if c["group"] and h % c["group"]:
+        c["group"] = 8
+    pad_in, pad_out = c["pad_in"] // 8 * 8, c["pad_out"] // 8 * 8
+    inp = synth.fused_inputs(n, m, h, dt, seed=c["seed"], gemma=c["gemma"], residual=c["residual"])
+    parts = [_view(p, pad_in, dev)[1] for p in inp["partials"]]
+    res = _view(inp["residual"], pad_in, dev)[1] if c["residual"] else None
+    w = None if c["skip_norm"] else inp["weight"].to(dev)
+    t16 = TDT[dt]
+    ro = _view(torch.empty((m, h), dtype=t16), pad_out, dev, fill=0xA5)[1]
+    y = _view(torch.empty((m, h), dtype=torch.float32 if c["out_fp32"] else t16), pad_out, dev, fill=0xA5)[1] \
+        if c["mirror"] else None
+    q = _view(torch.empty((m, h), dtype=torch.uint8), pad_out, dev, fill=0xA5)[1] if c["quant"] else None
+    sc = (torch.full((m, h // c["group"]) if c["group"] else (m,), float("nan"), dtype=torch.float32, device=dev)
+          if c["quant"] else None)
+    ptr = lambda t: None if t is None else t.data_ptr()
+    code = tar.AR_DTYPE_BF16 if dt == "bf16" else tar.AR_DTYPE_F16
+    args = tar.make_fused_args([p.data_ptr() for p in parts], ptr(res), ptr(ro), ptr(w), ptr(y), 1e-6, c["gemma"],
+                               c["quant"], ptr(q), ptr(sc), m, h, code, skip_norm=c["skip_norm"],
+                               out_fp32=c["out_fp32"], group_size=c["group"], ld_in=h + pad_in, ld_out=h + pad_out)
+    tar.ar_fused_reduce_rmsnorm_noalloc(args, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    if m == 0:
+        return
+    if y is None and c["skip_norm"]:
+        y = ro
+    _check_fused(orc, c, inp, ro.cpu(), None if y is None else y.cpu(), None if q is None else q.cpu(),
+                 None if sc is None else sc.cpu(), f"noalloc case {k} {c} h={h}")
