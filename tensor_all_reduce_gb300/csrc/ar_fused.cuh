@@ -12,7 +12,10 @@
 // contiguous chunk of 16-byte packs; each thread owns PPT packs strided by blockDim.
 // The row's square-sum and, with FP8, its amax are combined warp -> block (shared
 // memory) -> cluster (distributed shared memory).  Small-M decode shapes use csize > 1 so
-// that the few rows still spread over many SMs; large M uses csize = 1.
+// that the few rows still spread over many SMs; large M uses csize = 1.  On device memory the
+// staged kernel (ar_staged.cuh) takes every 16-byte-aligned row of up to 8192 elements; this
+// kernel serves buffers in host memory, rows that are not 16-byte aligned (VEC = false) and
+// rows longer than the staged cluster form takes, and runs when forced.
 //
 // VEC = true : every pack is a full, 16-byte-aligned group of 8 elements (h % 8 == 0 and
 //              all row starts aligned); one 128-bit load per pack and partial.
