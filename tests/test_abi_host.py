@@ -253,3 +253,19 @@ int main(void) {
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0 and r.stdout.strip() == f"ok {tar.AR_MAX_PARTIALS}", (r.returncode, r.stdout, r.stderr)
+
+
+def test_binding_constants_match_the_header():
+    """Every AR_* constant of the binding has the value include/ar.h gives it, and every valued
+    AR_* name of the header (enumerators and #defines) is mirrored in the binding."""
+    text = open(os.path.join(ROOT, "include", "ar.h")).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    header = {k: int(v) for k, v in re.findall(r"\b(AR_[A-Z0-9_]+)\s*=\s*(\d+)", text)}
+    header.update({k: int(v) for k, v in re.findall(r"#define\s+(AR_[A-Z0-9_]+)\s+(\d+)", text)})
+    assert len(header) >= 29
+    binding = {k: getattr(tar, k) for k in dir(tar) if k.startswith("AR_") and isinstance(getattr(tar, k), int)}
+    missing = sorted(set(header) - set(binding) - {"AR_NOALLOC_SCRATCH_BYTES"})
+    assert not missing, f"header constants without a binding mirror: {missing}"
+    wrong = {k: (binding[k], header[k]) for k in binding if k in header and binding[k] != header[k]}
+    assert not wrong, f"binding constants that differ from the header: {wrong}"
+    assert set(binding) <= set(header), sorted(set(binding) - set(header))
